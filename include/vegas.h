@@ -1,0 +1,160 @@
+/*
+ * vegas.h - C ABI of the Vegas hot path on one GB300 (sm_103a).
+ *
+ * Method: "Vegas: Self-Speculative Decoding with Verification-Guided Sparse
+ * Attention" (Yue, Xue, Huang), gist.science technical summary of paper
+ * 2602.07223.  One decode iteration runs
+ *   (1) full verify attention over the paged KV cache, capturing the
+ *       pre-softmax logits of the two Collect-2-Query rows summed per KV head
+ *       (§2 "Core mechanism", §2.A equation, §2.B "Collect-2-Query",
+ *       §3 "Implementation": logits taken before softmax normalisation);
+ *   (2) a per-(sequence, KV head) top-k over those summed logits (§2.A);
+ *   (3) gamma sparse draft-decode attention steps over the selected positions
+ *       plus a dense tail (§2, §3: PagedAttention with one token per page).
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer named "device" is a CUDA device pointer owned by the caller.
+ *    The library keeps no reference to it after the call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.  No entry point synchronises the host
+ *    except vegas_read_device_status.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns a status and launches nothing.  vegas_last_error_detail()
+ *    then describes it (per host thread).
+ *  - Faults only visible on the device (a block-table entry outside
+ *    [0, num_pages), a selected index outside the sequence, k_b > L_b, a
+ *    bounded wait that ran out) are recorded in a per-device error word; the
+ *    kernel clamps the access, skips the work and returns.  Nothing traps.
+ *    vegas_read_device_status() returns and clears that word.
+ *  - Workspaces are caller-allocated device memory of at least the size the
+ *    matching *_workspace_size() reports, zero-filled once before their first
+ *    use (e.g. cudaMemsetAsync).  Every call leaves the workspace's counters
+ *    at zero again.  A workspace must not be shared by calls that may run
+ *    concurrently.
+ *  - The library allocates no device memory in these calls.
+ */
+#ifndef VEGAS_H_
+#define VEGAS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VEGAS_ABI_VERSION 1
+#define VEGAS_PAGE_SIZE 16
+
+typedef enum {
+  VEGAS_OK = 0,
+  VEGAS_ERR_INVALID_ARG = 1,         /* host-side argument check failed; nothing launched */
+  VEGAS_ERR_UNSUPPORTED = 2,         /* valid but outside this build's supported shapes */
+  VEGAS_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the *_workspace_size() value */
+  VEGAS_ERR_CUDA = 4,                /* a CUDA runtime call failed (see detail string) */
+  VEGAS_ERR_DEVICE_FAULT = 5,        /* a kernel met an out-of-range page, index or k */
+  VEGAS_ERR_DEVICE_TIMEOUT = 6       /* a kernel's bounded wait ran out */
+} vegas_status_t;
+
+/*
+ * Paged KV cache (vLLM-style paging, §3).  K and V are separate bf16 tensors
+ * laid out [num_pages][num_kv_heads][page_size][head_dim], so one (page,
+ * KV head) block of 16 tokens is contiguous.  Logical position i of sequence b
+ * lives in physical page block_table[b * max_pages_per_seq + i / 16], slot
+ * i % 16.  Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ */
+typedef struct {
+  const void* k_cache;          /* device, bf16, 16-byte aligned */
+  const void* v_cache;          /* device, bf16, 16-byte aligned */
+  const int32_t* block_table;   /* device, int32 [batch][max_pages_per_seq] */
+  int32_t num_pages;
+  int32_t page_size;            /* must be 16 */
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;             /* 64 or 128 */
+  int32_t max_pages_per_seq;
+} vegas_paged_kv_t;
+
+/* ------------------------------------------------------------------------
+ * (1) Verify attention with Collect-2-Query capture.
+ *
+ * For sequence b with committed prefix L_b = ctx_lens[b] and window row
+ * t in [0, gamma] (the window's K/V already sit at positions L_b .. L_b+gamma),
+ * query head h attends positions [0, L_b + t]:
+ *   l_ti = (q_t^h . k_i) * softmax_scale,  o_t^h = sum_i softmax(l)_i v_i.
+ * If scores != NULL, also writes, for every KV head g and i in [0, L_b),
+ *   scores[(b * num_kv_heads + g) * score_stride + i]
+ *     = sum_{t in {capture_row_a, capture_row_b}} sum_{h in group g} l_ti^(h)
+ * (fp32; the §2.A objective restricted to the two Collect-2-Query rows,
+ * rows 0 and gamma under this library's reading).  capture_row_a ==
+ * capture_row_b captures one row once.  Entries at i >= L_b are not written.
+ *
+ *   q:   device bf16 [batch][gamma + 1][num_q_heads][head_dim]
+ *   out: device bf16, same shape as q
+ *   ctx_lens: device int32 [batch]; needs L_b + gamma + 1 <= 16 * max_pages_per_seq
+ *   score_stride >= max_b L_b when scores != NULL
+ * Supported: head_dim in {64, 128}; (gamma + 1) * G <= 64 with G = Hq / Hkv;
+ * gamma in [0, 15].
+ * ---------------------------------------------------------------------- */
+size_t vegas_verify_workspace_size(const vegas_paged_kv_t* kv, int batch, int gamma);
+
+vegas_status_t vegas_verify_attn_capture(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
+    int score_stride, const int32_t* ctx_lens, int batch, int gamma,
+    int capture_row_a, int capture_row_b, float softmax_scale,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (2) Top-k select (§2.A argmax over |T| = k of the summed logits).
+ *
+ * For every (b, g): the k_b = k_per_seq[b] positions i in [0, L_b) of
+ * largest scores[(b * num_kv_heads + g) * score_stride + i], ties going to
+ * the lower position, written ascending to
+ * out_idx[(b * num_kv_heads + g) * k_max + j], j < k_b; entries j >= k_b are
+ * set to -1.  -0.0 ranks equal to +0.0.  NaN scores are outside the
+ * contract (they rank lowest).  Needs 0 <= k_b <= min(L_b, k_max) and
+ * L_b <= score_stride <= 524288.
+ * ---------------------------------------------------------------------- */
+vegas_status_t vegas_select_topk(
+    const float* scores, int score_stride, const int32_t* ctx_lens,
+    const int32_t* k_per_seq, int32_t* out_idx, int batch, int num_kv_heads,
+    int k_max, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (3) Sparse draft-decode attention, one draft step (§2, §3).
+ *
+ * For every b and query head h (KV head g = h / G), attends the positions
+ *   idx[(b * num_kv_heads + g) * k_max + j] for j < k_per_seq[b]
+ *   followed by tail_start[b] .. tail_start[b] + tail_len[b] - 1
+ * with o = sum softmax((q . k_i) * softmax_scale) v_i.  idx entries are
+ * logical positions (page size 1 semantics); each must lie inside the
+ * block table's range.
+ *   q, out: device bf16 [batch][num_q_heads][head_dim]
+ *   max_tail >= max_b tail_len[b]; k_per_seq[b] + tail_len[b] >= 1.
+ * Supported: head_dim in {64, 128}, G <= 16.
+ * ---------------------------------------------------------------------- */
+size_t vegas_sparse_workspace_size(const vegas_paged_kv_t* kv, int batch, int k_max,
+                                   int max_tail);
+
+vegas_status_t vegas_sparse_decode_attn(
+    const vegas_paged_kv_t* kv, const void* q, void* out, const int32_t* idx,
+    int k_max, const int32_t* k_per_seq, const int32_t* tail_start,
+    const int32_t* tail_len, int max_tail, int batch, float softmax_scale,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Status.
+ * ---------------------------------------------------------------------- */
+/* Synchronises `stream`, returns the current device's error word as a status
+ * (VEGAS_OK when clear) and clears it. */
+vegas_status_t vegas_read_device_status(void* stream);
+const char* vegas_status_string(vegas_status_t status);
+/* Human-readable detail of the last non-OK status returned on this host thread. */
+const char* vegas_last_error_detail(void);
+int vegas_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VEGAS_H_ */

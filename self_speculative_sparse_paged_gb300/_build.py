@@ -1,0 +1,87 @@
+"""Builds libvegas.so (the Vegas hot-path kernels and their C ABI) in-tree.
+
+nvcc compiles each translation unit for sm_103a in parallel; the verify kernel
+source is compiled once per (head_dim, capture) pair so its 28 instantiations
+spread over four units.  Objects are rebuilt only when a source or header is
+newer than the library.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(BUILD, "libvegas.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+                "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]
+
+UNITS = [
+    ("vegas_api.cu", "vegas_api.o", []),
+    ("synth.cu", "synth.o", []),
+    ("select_topk.cu", "select_topk.o", []),
+    ("sparse_decode.cu", "sparse_decode.o", []),
+    ("verify_attn.cu", "verify_d128_c1.o", ["-DVEGAS_D=128", "-DVEGAS_CAP=1"]),
+    ("verify_attn.cu", "verify_d128_c0.o", ["-DVEGAS_D=128", "-DVEGAS_CAP=0"]),
+    ("verify_attn.cu", "verify_d64_c1.o", ["-DVEGAS_D=64", "-DVEGAS_CAP=1"]),
+    ("verify_attn.cu", "verify_d64_c0.o", ["-DVEGAS_D=64", "-DVEGAS_CAP=0"]),
+]
+
+
+def nvcc() -> str:
+    cand = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(cand):
+        raise RuntimeError("nvcc not found: the Vegas CUDA library cannot be built")
+    return cand
+
+
+def _sources_mtime() -> float:
+    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    paths += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+    paths.append(os.path.abspath(__file__))
+    return max(os.path.getmtime(p) for p in paths)
+
+
+def up_to_date() -> bool:
+    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _sources_mtime()
+
+
+def build(verbose: bool = False, jobs: int | None = None) -> str:
+    """Compile every unit for sm_103a and link libvegas.so; returns its path."""
+    if up_to_date():
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    cc = nvcc()
+
+    def compile_unit(unit):
+        src, obj, extra = unit
+        cmd = [cc] + FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", os.path.join(BUILD, obj)]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src} {' '.join(extra)}:\n{r.stdout}\n{r.stderr}")
+        if verbose:
+            sys.stdout.write(f"built {obj}\n")
+        return obj
+
+    jobs = jobs or min(len(UNITS), max(1, os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=jobs) as ex:
+        objs = list(ex.map(compile_unit, UNITS))
+    tmp = LIB + ".tmp"
+    cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [os.path.join(BUILD, o) for o in objs]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose=True))

@@ -1,0 +1,90 @@
+// Host-side launch interface of the Vegas kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vegas {
+
+constexpr int kAttnWarps = 8;          // warps per attention CTA
+constexpr int kMaxSplits = 128;        // split-KV partials per (sequence, KV head)
+
+struct VerifyParams {
+  const void* q;            // bf16 [B][T][Hq][D]
+  void* out;                // bf16 [B][T][Hq][D]
+  float* scores;            // fp32 [B][Hkv][score_stride] or null
+  const int32_t* ctx_lens;  // [B]
+  const int32_t* block_table;
+  int score_stride;
+  int num_pages;
+  int max_pages;
+  int hq, hkv, group, gamma, nq;
+  int row_a, row_b;
+  float scale;              // softmax scale (logit units)
+  float scale_log2;         // scale * log2(e)
+  int pages_per_split;
+  int num_splits;
+  int* tickets;
+  float* part_ml;
+  float* part_o;
+  int* err;
+};
+
+struct SparseParams {
+  const void* q;            // bf16 [B][Hq][D]
+  void* out;                // bf16 [B][Hq][D]
+  const void* k_cache;      // bf16 [pages][Hkv][16][D]
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* idx;       // [B][Hkv][k_max]
+  const int32_t* k_per_seq;
+  const int32_t* tail_start;
+  const int32_t* tail_len;
+  int k_max;
+  int num_pages, max_pages;
+  int hq, hkv, group;
+  float scale_log2;
+  int rows_per_split;
+  int num_splits;
+  int* tickets;
+  float* part_ml;
+  float* part_o;
+  int* err;
+};
+
+struct SelectParams {
+  const float* scores;
+  const int32_t* ctx_lens;
+  const int32_t* k_per_seq;
+  int32_t* out_idx;
+  int score_stride;
+  int hkv;
+  int k_max;
+  int chunk;                // keys per CTA of a cluster
+  int* err;
+};
+
+// Shared-memory bytes and launch of each kernel; return cudaError_t.
+
+// Largest 8-row query tile count per head_dim (d=128: 48 rows, d=64: 64 rows).
+inline int verify_max_ntiles(int head_dim) { return head_dim == 128 ? 6 : 8; }
+template <int D, bool CAP>
+cudaError_t launch_verify_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            const VerifyParams& p, int ntiles, int batch, cudaStream_t stream);
+
+size_t sparse_smem_bytes(int head_dim, int ntiles);
+int sparse_max_rows_per_split();
+cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int batch,
+                          cudaStream_t stream);
+
+int select_max_chunk();
+cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream);
+
+cudaError_t launch_synth_kv(void* cache, int which, uint64_t seed, int layer, const int32_t* owner,
+                            int num_pages, int hkv, int head_dim, int max_pages,
+                            const int32_t* ctx_lens, const int32_t* positions,
+                            uint64_t heavy_threshold, int heavy_last, const float* unit_dir,
+                            cudaStream_t stream);
+
+}  // namespace vegas

@@ -1,0 +1,215 @@
+// Sparse draft-decode attention: one draft step over the selected positions.
+//
+// "Vegas: Self-Speculative Decoding with Verification-Guided Sparse
+// Attention", gist.science technical summary: §2 "Core mechanism" (the draft
+// phase attends only to the critical KV entries selected from the previous
+// verification) and §3 "Implementation" (PagedAttention with a page size of
+// one token, the selected token indices passed as page indices).
+//
+// Here the selected positions stay logical token positions: each is mapped
+// through the block table of the 16-token paged cache, so the same cache
+// serves verify and draft.  Grid (num_splits, Hkv, B); a CTA owns a
+// contiguous range of the unit's list "T then tail".  It first resolves every
+// entry of its range to a cache row (position -> page -> row) in shared
+// memory, then each warp gathers 16-entry groups with one 1-D bulk copy per
+// K row and per V row (lanes 0-15 K, 16-31 V) into padded rows, and runs the
+// same warp core as the verify kernel with the G query heads of the group as
+// the tile's columns.
+#include "kernels.h"
+#include "split_merge.cuh"
+
+namespace vegas {
+
+template <int D>
+struct SparseCfg {
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kRow = D * 2 + 16;           // padded row stride
+  static constexpr int kTile = 16 * kRow;
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kMaxRowsPerSplit = 1024;
+};
+
+template <int D, int NT>
+constexpr size_t sparse_smem_layout_bytes() {
+  return size_t(kAttnWarps) * SparseCfg<D>::kStages * SparseCfg<D>::kStage   // stages
+         + size_t(NT) * 8 * (2 * D + 16)                                     // Q tile
+         + size_t(kAttnWarps) * SparseCfg<D>::kStages * 8                    // mbarriers
+         + size_t(SparseCfg<D>::kMaxRowsPerSplit) * 4                        // row table
+         + 1024;
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const SparseParams p) {
+  constexpr int W = kAttnWarps;
+  constexpr int NPAD = NT * 8;
+  constexpr int STAGES = SparseCfg<D>::kStages;
+  constexpr int ROW = SparseCfg<D>::kRow;
+  constexpr int TILE = SparseCfg<D>::kTile;
+  constexpr int STAGE = SparseCfg<D>::kStage;
+  constexpr int QROW = 2 * D + 16;
+  using Tile = PaddedTile<D>;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stage_area = smem;
+  uint8_t* qs = smem + W * STAGES * STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qs + NPAD * QROW);
+  int32_t* rows = reinterpret_cast<int32_t*>(bars + W * STAGES);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int unit = b * p.hkv + g;
+  const int cap = p.max_pages * 16;
+
+  int kb = p.k_per_seq[b];
+  if (kb < 0 || kb > p.k_max) {
+    if (tid == 0 && g == 0 && split == 0) set_error(p.err, kErrDeviceFault);
+    kb = max(0, min(kb, p.k_max));
+  }
+  const int tstart = p.tail_start[b];
+  const int tlen = max(0, p.tail_len[b]);
+  const int total = kb + tlen;
+  const int rbeg = split * p.rows_per_split;
+  const int rend = min(rbeg + p.rows_per_split, total);
+  const int nrows = max(0, rend - rbeg);
+
+  if (tid == 0) {
+    for (int i = 0; i < W * STAGES; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    fence_mbar_init();
+  }
+  // Entry e of the list: T[e] for e < k_b, else tail_start + (e - k_b).
+  for (int i = tid; i < nrows; i += W * 32) {
+    const int e = rbeg + i;
+    int pos = e < kb ? p.idx[size_t(unit) * p.k_max + e] : tstart + (e - kb);
+    if (pos < 0 || pos >= cap) {
+      set_error(p.err, kErrDeviceFault);
+      pos = 0;
+    }
+    int phys = p.block_table[size_t(b) * p.max_pages + (pos >> 4)];
+    if (phys < 0 || phys >= p.num_pages) {
+      set_error(p.err, kErrDeviceFault);
+      phys = 0;
+    }
+    rows[i] = (phys * p.hkv + g) * 16 + (pos & 15);
+  }
+  for (int i = tid; i < NPAD * (D / 8); i += W * 32) {
+    const int n = i / (D / 8), c = i % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (n < p.group) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t(b) * p.hq + g * p.group + n) * D);
+      v = src[c];
+    }
+    *reinterpret_cast<uint4*>(qs + n * QROW + c * 16) = v;
+  }
+  __syncthreads();
+
+  const int ngroups = (nrows + 15) / 16;
+  const int nmy = warp < ngroups ? (ngroups - warp + W - 1) / W : 0;
+  const uint32_t stage0 = smem_u32(stage_area + warp * STAGES * STAGE);
+  const uint32_t bar0 = smem_u32(&bars[warp * STAGES]);
+  const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(p.k_cache);
+  const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(p.v_cache);
+
+  // Every lane issues one row copy; rows past the range repeat the group's
+  // first row (masked later) so the byte count per stage is constant.
+  auto issue = [&](int i) {
+    const int grp = warp + i * W;
+    const int s = i % STAGES;
+    const uint32_t bar = bar0 + s * 8;
+    if (lane == 0) mbar_arrive_expect_tx(bar, 32 * D * 2);   // 32 rows of D bf16
+    __syncwarp();
+    const int r = lane & 15;
+    const int li = grp * 16 + r;
+    const int row = rows[li < nrows ? li : grp * 16];
+    const __nv_bfloat16* src = (lane < 16 ? kc : vc) + size_t(row) * D;
+    const uint32_t dst = stage0 + s * STAGE + (lane < 16 ? 0 : TILE) + r * ROW;
+    bulk_load(dst, src, D * 2, bar);
+  };
+  for (int i = 0; i < min(STAGES, nmy); ++i) issue(i);
+
+  uint32_t qf[D / 16][NT][2];
+  load_q_frags<D, NT>(smem_u32(qs), qf);
+  WarpState<D, NT> st;
+  st.init();
+
+  int done = 0;
+  bool ok = true;
+  for (; done < nmy; ++done) {
+    const int i = done;
+    const int s = i % STAGES;
+    if (!mbar_wait_bounded(bar0 + s * 8, (i / STAGES) & 1)) {
+      ok = false;
+      break;
+    }
+    const int grp = warp + i * W;
+    const uint32_t kb_s = stage0 + s * STAGE;
+    float sc[NT][4];
+    tile_scores<D, NT, Tile>(kb_s, qf, sc);
+    float x[NT][4];
+    const int valid = nrows - grp * 16;   // rows of this group inside the range
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = (lane >> 2) + 8 * (k >> 1);
+        x[nt][k] = r < valid ? sc[nt][k] * p.scale_log2 : -INFINITY;
+      }
+    tile_softmax_pv<D, NT, Tile>(st, x, kb_s + TILE);
+    __syncwarp();
+    if (i + STAGES < nmy) {
+      fence_proxy_async_smem();
+      issue(i + STAGES);
+    }
+  }
+  if (!ok) {
+    if (lane == 0) set_error(p.err, kErrDeviceTimeout);
+    for (int j = done; j < min(done + STAGES, nmy); ++j)
+      (void)mbar_wait_bounded(bar0 + (j % STAGES) * 8, (j / STAGES) & 1);
+  }
+  reduce_row_sums<D, NT>(st);
+  __syncthreads();
+
+  SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+  auto out_row = [&](int n) { return out + (size_t(b) * p.hq + g * p.group + n) * D; };
+  merge_and_write<D, NT, W>(st, stage_area, size_t(W) * STAGES * STAGE, p.group, unit, split,
+                            p.num_splits, ws, out_row);
+}
+
+size_t sparse_smem_bytes(int head_dim, int ntiles) {
+  (void)ntiles;
+  return head_dim == 128 ? sparse_smem_layout_bytes<128, 2>() : sparse_smem_layout_bytes<64, 2>();
+}
+
+int sparse_max_rows_per_split() { return SparseCfg<128>::kMaxRowsPerSplit; }
+
+template <int D, int NT>
+static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStream_t stream) {
+  const size_t smem = sparse_smem_bytes(D, NT);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<D, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(p.num_splits, p.hkv, batch);
+  sparse_decode_kernel<D, NT><<<grid, kAttnWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int batch,
+                          cudaStream_t stream) {
+  if (head_dim == 128) {
+    if (ntiles == 1) return launch_sparse_one<128, 1>(p, batch, stream);
+    if (ntiles == 2) return launch_sparse_one<128, 2>(p, batch, stream);
+  } else if (head_dim == 64) {
+    if (ntiles == 1) return launch_sparse_one<64, 1>(p, batch, stream);
+    if (ntiles == 2) return launch_sparse_one<64, 2>(p, batch, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace vegas

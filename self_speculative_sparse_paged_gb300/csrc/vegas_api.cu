@@ -1,0 +1,459 @@
+// C ABI of the Vegas hot path: host-side validation, launch configuration,
+// TMA descriptors and the device error word.  Declarations and contracts are
+// in include/vegas.h and include/vegas_synth.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/vegas.h"
+#include "../../include/vegas_synth.h"
+#include "kernels.h"
+
+#define VEGAS_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+__device__ int g_error_word;   // one per device; kernels record the first fault here
+
+thread_local char g_detail[512] = "";
+
+vegas_status_t fail(vegas_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+vegas_status_t cuda_fail(cudaError_t e, const char* where) {
+  return fail(VEGAS_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+// Device address of the error word and SM count of the current device.
+vegas_status_t device_info(int** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(VEGAS_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_sms[dev] = n;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (sms) *sms = g_sms[dev];
+  return VEGAS_OK;
+}
+
+int current_sms() {
+  int sms = 0;
+  if (device_info(nullptr, &sms) != VEGAS_OK || sms <= 0) sms = 148;
+  return sms;
+}
+
+// ----------------------------------------------------------------- TMA maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+vegas_status_t get_encoder(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                           &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = (EncodeTiledFn)p;
+  });
+  if (!cached) return fail(VEGAS_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)",
+                           cudaGetErrorString(err));
+  *fn = cached;
+  return VEGAS_OK;
+}
+
+// 2-D view of a paged cache: rows = num_pages * Hkv * 16, head_dim bf16 each;
+// box 16 rows x 64 elements (128 bytes), 128-byte swizzle.
+vegas_status_t make_cache_map(CUtensorMap* map, const void* base, const vegas_paged_kv_t* kv) {
+  EncodeTiledFn enc;
+  vegas_status_t st = get_encoder(&enc);
+  if (st != VEGAS_OK) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)kv->head_dim,
+                        (cuuint64_t)kv->num_pages * kv->num_kv_heads * VEGAS_PAGE_SIZE};
+  cuuint64_t strides[1] = {(cuuint64_t)kv->head_dim * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(VEGAS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return VEGAS_OK;
+}
+
+// ----------------------------------------------------------------- checks
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+vegas_status_t check_kv(const vegas_paged_kv_t* kv) {
+  if (!kv) return fail(VEGAS_ERR_INVALID_ARG, "kv is NULL");
+  if (!kv->k_cache || !kv->v_cache || !kv->block_table)
+    return fail(VEGAS_ERR_INVALID_ARG, "kv: NULL cache or block table");
+  if (!aligned16(kv->k_cache) || !aligned16(kv->v_cache))
+    return fail(VEGAS_ERR_INVALID_ARG, "kv: caches must be 16-byte aligned");
+  if (kv->page_size != VEGAS_PAGE_SIZE)
+    return fail(VEGAS_ERR_UNSUPPORTED, "page_size %d (only 16)", kv->page_size);
+  if (kv->head_dim != 64 && kv->head_dim != 128)
+    return fail(VEGAS_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", kv->head_dim);
+  if (kv->num_kv_heads < 1 || kv->num_q_heads < 1 || kv->num_q_heads % kv->num_kv_heads)
+    return fail(VEGAS_ERR_INVALID_ARG, "heads: Hq %d must be a positive multiple of Hkv %d",
+                kv->num_q_heads, kv->num_kv_heads);
+  if (kv->num_pages < 1 || kv->max_pages_per_seq < 1)
+    return fail(VEGAS_ERR_INVALID_ARG, "num_pages %d / max_pages_per_seq %d", kv->num_pages,
+                kv->max_pages_per_seq);
+  if ((long long)kv->num_pages * kv->num_kv_heads * VEGAS_PAGE_SIZE >= (1ll << 31))
+    return fail(VEGAS_ERR_UNSUPPORTED, "cache rows (num_pages * Hkv * 16) must be < 2^31");
+  if ((long long)kv->max_pages_per_seq * VEGAS_PAGE_SIZE >= (1ll << 24))
+    return fail(VEGAS_ERR_UNSUPPORTED, "sequence capacity must be < 2^24 positions");
+  return VEGAS_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Splits per (sequence, KV head): fill whole waves of one CTA per SM.
+int verify_splits(int units, int max_pages, int sms) {
+  const int s0 = (sms + units - 1) / units;
+  int best = 1;
+  double best_eff = -1.0;
+  const int hi = std::min(std::min(4 * s0, vegas::kMaxSplits), std::max(1, max_pages / 8));
+  for (int s = std::max(1, std::min(s0, hi)); s <= hi; ++s) {
+    const long long ctas = (long long)units * s;
+    const long long waves = (ctas + sms - 1) / sms;
+    const double eff = double(ctas) / double(waves * sms);
+    if (eff > best_eff + 1e-9) {
+      best = s;
+      best_eff = eff;
+    }
+    if (eff >= 0.999) break;
+  }
+  return best;
+}
+
+struct VerifyPlan {
+  int nq, ntiles, splits, pages_per_split;
+  size_t tickets_off, ml_off, o_off, bytes;
+};
+
+VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms) {
+  VerifyPlan pl{};
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  pl.nq = (gamma + 1) * G;
+  pl.ntiles = (pl.nq + 7) / 8;
+  const int units = std::max(1, batch * kv->num_kv_heads);
+  pl.splits = verify_splits(units, kv->max_pages_per_seq, sms);
+  pl.pages_per_split = (kv->max_pages_per_seq + pl.splits - 1) / pl.splits;
+  pl.splits = (kv->max_pages_per_seq + pl.pages_per_split - 1) / pl.pages_per_split;
+  pl.tickets_off = 0;
+  pl.ml_off = align256(size_t(units) * 4);
+  pl.o_off = pl.ml_off + align256(size_t(units) * pl.splits * pl.nq * 2 * 4);
+  pl.bytes = pl.o_off + size_t(units) * pl.splits * pl.nq * kv->head_dim * 4;
+  return pl;
+}
+
+struct SparsePlan {
+  int ntiles, splits, rows_per_split;
+  size_t tickets_off, ml_off, o_off, bytes;
+};
+
+SparsePlan plan_sparse(const vegas_paged_kv_t* kv, int batch, int k_max, int max_tail, int sms) {
+  SparsePlan pl{};
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  pl.ntiles = (G + 7) / 8;
+  const int units = std::max(1, batch * kv->num_kv_heads);
+  const int rows_max = std::max(1, k_max + max_tail);
+  const int cap = vegas::sparse_max_rows_per_split();
+  int s = std::max((sms + units - 1) / units, (rows_max + cap - 1) / cap);
+  s = std::min(s, std::max(1, (rows_max + 15) / 16));
+  s = std::min(s, vegas::kMaxSplits);
+  int rps = (rows_max + s - 1) / s;
+  rps = (rps + 15) / 16 * 16;
+  pl.rows_per_split = rps;
+  pl.splits = (rows_max + rps - 1) / rps;
+  pl.tickets_off = 0;
+  pl.ml_off = align256(size_t(units) * 4);
+  pl.o_off = pl.ml_off + align256(size_t(units) * pl.splits * G * 2 * 4);
+  pl.bytes = pl.o_off + size_t(units) * pl.splits * G * kv->head_dim * 4;
+  return pl;
+}
+
+cudaError_t launch_verify_any(const CUtensorMap& km, const CUtensorMap& vm,
+                              const vegas::VerifyParams& p, int d, int nt, bool cap, int batch,
+                              cudaStream_t s) {
+  if (d == 128)
+    return cap ? vegas::launch_verify_t<128, true>(km, vm, p, nt, batch, s)
+               : vegas::launch_verify_t<128, false>(km, vm, p, nt, batch, s);
+  return cap ? vegas::launch_verify_t<64, true>(km, vm, p, nt, batch, s)
+             : vegas::launch_verify_t<64, false>(km, vm, p, nt, batch, s);
+}
+
+}  // namespace
+
+// =========================================================================
+// Verify attention with Collect-2-Query capture
+// =========================================================================
+VEGAS_API size_t vegas_verify_workspace_size(const vegas_paged_kv_t* kv, int batch, int gamma) {
+  if (check_kv(kv) != VEGAS_OK || batch < 0 || gamma < 0) return 0;
+  return plan_verify(kv, batch, gamma, current_sms()).bytes;
+}
+
+VEGAS_API vegas_status_t vegas_verify_attn_capture(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* scores, int score_stride,
+    const int32_t* ctx_lens, int batch, int gamma, int capture_row_a, int capture_row_b,
+    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  vegas_status_t st = check_kv(kv);
+  if (st != VEGAS_OK) return st;
+  if (batch < 0) return fail(VEGAS_ERR_INVALID_ARG, "batch %d", batch);
+  if (gamma < 0 || gamma > 15) return fail(VEGAS_ERR_UNSUPPORTED, "gamma %d (0..15)", gamma);
+  if (!q || !out || !ctx_lens) return fail(VEGAS_ERR_INVALID_ARG, "NULL q, out or ctx_lens");
+  if (!aligned16(q)) return fail(VEGAS_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!std::isfinite(softmax_scale)) return fail(VEGAS_ERR_INVALID_ARG, "softmax_scale not finite");
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  const int nq = (gamma + 1) * G;
+  if ((nq + 7) / 8 > vegas::verify_max_ntiles(kv->head_dim))
+    return fail(VEGAS_ERR_UNSUPPORTED, "(gamma+1)*G = %d query rows exceeds %d for head_dim %d", nq,
+                8 * vegas::verify_max_ntiles(kv->head_dim), kv->head_dim);
+  if (scores) {
+    if (score_stride < 1) return fail(VEGAS_ERR_INVALID_ARG, "score_stride %d", score_stride);
+    if (capture_row_a < 0 || capture_row_a > gamma || capture_row_b < 0 || capture_row_b > gamma)
+      return fail(VEGAS_ERR_INVALID_ARG, "capture rows (%d, %d) outside [0, %d]", capture_row_a,
+                  capture_row_b, gamma);
+  }
+  if (batch == 0) return VEGAS_OK;
+  int* err = nullptr;
+  int sms = 0;
+  if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
+  const VerifyPlan pl = plan_verify(kv, batch, gamma, sms);
+  if (pl.splits > 1) {
+    if (!workspace || workspace_bytes < pl.bytes)
+      return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "verify workspace %zu < %zu bytes",
+                  workspace_bytes, pl.bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(VEGAS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  CUtensorMap km, vm;
+  if ((st = make_cache_map(&km, kv->k_cache, kv)) != VEGAS_OK) return st;
+  if ((st = make_cache_map(&vm, kv->v_cache, kv)) != VEGAS_OK) return st;
+  vegas::VerifyParams p{};
+  p.q = q;
+  p.out = out;
+  p.scores = scores;
+  p.ctx_lens = ctx_lens;
+  p.block_table = kv->block_table;
+  p.score_stride = score_stride;
+  p.num_pages = kv->num_pages;
+  p.max_pages = kv->max_pages_per_seq;
+  p.hq = kv->num_q_heads;
+  p.hkv = kv->num_kv_heads;
+  p.group = G;
+  p.gamma = gamma;
+  p.nq = nq;
+  p.row_a = capture_row_a;
+  p.row_b = capture_row_b;
+  p.scale = softmax_scale;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.pages_per_split = pl.pages_per_split;
+  p.num_splits = pl.splits;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.tickets = ws ? reinterpret_cast<int*>(ws + pl.tickets_off) : nullptr;
+  p.part_ml = ws ? reinterpret_cast<float*>(ws + pl.ml_off) : nullptr;
+  p.part_o = ws ? reinterpret_cast<float*>(ws + pl.o_off) : nullptr;
+  p.err = err;
+  cudaError_t e = launch_verify_any(km, vm, p, kv->head_dim, pl.ntiles, scores != nullptr, batch,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  return VEGAS_OK;
+}
+
+// =========================================================================
+// Top-k select
+// =========================================================================
+VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride,
+                                           const int32_t* ctx_lens, const int32_t* k_per_seq,
+                                           int32_t* out_idx, int batch, int num_kv_heads,
+                                           int k_max, void* stream) {
+  if (!scores || !ctx_lens || !k_per_seq || !out_idx)
+    return fail(VEGAS_ERR_INVALID_ARG, "NULL pointer argument");
+  if (batch < 0 || num_kv_heads < 1 || k_max < 0 || score_stride < 1)
+    return fail(VEGAS_ERR_INVALID_ARG, "batch %d, num_kv_heads %d, k_max %d, score_stride %d",
+                batch, num_kv_heads, k_max, score_stride);
+  const int max_chunk = vegas::select_max_chunk();
+  if ((long long)score_stride > 16ll * max_chunk)
+    return fail(VEGAS_ERR_UNSUPPORTED, "score_stride %d exceeds %d", score_stride, 16 * max_chunk);
+  if (batch == 0 || k_max == 0) return VEGAS_OK;
+  int* err = nullptr;
+  int sms = 0;
+  vegas_status_t st = device_info(&err, &sms);
+  if (st != VEGAS_OK) return st;
+  const int units = batch * num_kv_heads;
+  int cl = 1;
+  while ((score_stride + cl - 1) / cl > max_chunk) cl *= 2;
+  while (cl < 8 && units * cl * 2 <= sms && (score_stride + 2 * cl - 1) / (2 * cl) >= 1024) cl *= 2;
+  vegas::SelectParams p{};
+  p.scores = scores;
+  p.ctx_lens = ctx_lens;
+  p.k_per_seq = k_per_seq;
+  p.out_idx = out_idx;
+  p.score_stride = score_stride;
+  p.hkv = num_kv_heads;
+  p.k_max = k_max;
+  p.chunk = (score_stride + cl - 1) / cl;
+  p.err = err;
+  cudaError_t e = vegas::launch_select(p, cl, batch, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  return VEGAS_OK;
+}
+
+// =========================================================================
+// Sparse draft-decode attention
+// =========================================================================
+VEGAS_API size_t vegas_sparse_workspace_size(const vegas_paged_kv_t* kv, int batch, int k_max,
+                                             int max_tail) {
+  if (check_kv(kv) != VEGAS_OK || batch < 0 || k_max < 0 || max_tail < 0) return 0;
+  return plan_sparse(kv, batch, k_max, max_tail, current_sms()).bytes;
+}
+
+VEGAS_API vegas_status_t vegas_sparse_decode_attn(
+    const vegas_paged_kv_t* kv, const void* q, void* out, const int32_t* idx, int k_max,
+    const int32_t* k_per_seq, const int32_t* tail_start, const int32_t* tail_len, int max_tail,
+    int batch, float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  vegas_status_t st = check_kv(kv);
+  if (st != VEGAS_OK) return st;
+  if (batch < 0 || k_max < 0 || max_tail < 0)
+    return fail(VEGAS_ERR_INVALID_ARG, "batch %d, k_max %d, max_tail %d", batch, k_max, max_tail);
+  if (k_max + max_tail < 1) return fail(VEGAS_ERR_INVALID_ARG, "empty attention set");
+  if (!q || !out || !k_per_seq || !tail_start || !tail_len || (k_max > 0 && !idx))
+    return fail(VEGAS_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned16(q)) return fail(VEGAS_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!std::isfinite(softmax_scale)) return fail(VEGAS_ERR_INVALID_ARG, "softmax_scale not finite");
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  if (G > 16) return fail(VEGAS_ERR_UNSUPPORTED, "group size %d (at most 16)", G);
+  if (batch == 0) return VEGAS_OK;
+  int* err = nullptr;
+  int sms = 0;
+  if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
+  const SparsePlan pl = plan_sparse(kv, batch, k_max, max_tail, sms);
+  if (pl.splits > 1) {
+    if (!workspace || workspace_bytes < pl.bytes)
+      return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "sparse workspace %zu < %zu bytes",
+                  workspace_bytes, pl.bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(VEGAS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  vegas::SparseParams p{};
+  p.q = q;
+  p.out = out;
+  p.k_cache = kv->k_cache;
+  p.v_cache = kv->v_cache;
+  p.block_table = kv->block_table;
+  p.idx = idx;
+  p.k_per_seq = k_per_seq;
+  p.tail_start = tail_start;
+  p.tail_len = tail_len;
+  p.k_max = k_max;
+  p.num_pages = kv->num_pages;
+  p.max_pages = kv->max_pages_per_seq;
+  p.hq = kv->num_q_heads;
+  p.hkv = kv->num_kv_heads;
+  p.group = G;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.rows_per_split = pl.rows_per_split;
+  p.num_splits = pl.splits;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.tickets = ws ? reinterpret_cast<int*>(ws + pl.tickets_off) : nullptr;
+  p.part_ml = ws ? reinterpret_cast<float*>(ws + pl.ml_off) : nullptr;
+  p.part_o = ws ? reinterpret_cast<float*>(ws + pl.o_off) : nullptr;
+  p.err = err;
+  cudaError_t e = vegas::launch_sparse(p, kv->head_dim, pl.ntiles, batch,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse launch");
+  return VEGAS_OK;
+}
+
+// =========================================================================
+// Synthetic input generator
+// =========================================================================
+VEGAS_API vegas_status_t vegas_synth_paged_kv(void* cache, int which, uint64_t seed, int layer,
+                                              const int32_t* owner, int num_pages,
+                                              int num_kv_heads, int head_dim,
+                                              int max_pages_per_seq, const int32_t* ctx_lens,
+                                              const int32_t* positions, uint64_t heavy_threshold,
+                                              int heavy_last, const float* unit_dir,
+                                              void* stream) {
+  if (!cache || !owner || !ctx_lens || !positions || !unit_dir)
+    return fail(VEGAS_ERR_INVALID_ARG, "NULL pointer argument");
+  if ((which != 0 && which != 1) || layer < 0 || num_pages < 1 || num_kv_heads < 1 ||
+      (head_dim != 64 && head_dim != 128) || max_pages_per_seq < 1 || heavy_last < 0)
+    return fail(VEGAS_ERR_INVALID_ARG, "bad generator shape");
+  if (!aligned16(cache)) return fail(VEGAS_ERR_INVALID_ARG, "cache must be 16-byte aligned");
+  cudaError_t e = vegas::launch_synth_kv(cache, which, seed, layer, owner, num_pages, num_kv_heads,
+                                         head_dim, max_pages_per_seq, ctx_lens, positions,
+                                         heavy_threshold, heavy_last, unit_dir,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "synth launch");
+  return VEGAS_OK;
+}
+
+// =========================================================================
+// Status
+// =========================================================================
+VEGAS_API vegas_status_t vegas_read_device_status(void* stream) {
+  int* err = nullptr;
+  vegas_status_t st = device_info(&err, nullptr);
+  if (st != VEGAS_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (word != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    return fail(static_cast<vegas_status_t>(word), "device reported %s",
+                vegas_status_string(static_cast<vegas_status_t>(word)));
+  }
+  return VEGAS_OK;
+}
+
+VEGAS_API const char* vegas_status_string(vegas_status_t s) {
+  switch (s) {
+    case VEGAS_OK: return "VEGAS_OK";
+    case VEGAS_ERR_INVALID_ARG: return "VEGAS_ERR_INVALID_ARG";
+    case VEGAS_ERR_UNSUPPORTED: return "VEGAS_ERR_UNSUPPORTED";
+    case VEGAS_ERR_WORKSPACE_TOO_SMALL: return "VEGAS_ERR_WORKSPACE_TOO_SMALL";
+    case VEGAS_ERR_CUDA: return "VEGAS_ERR_CUDA";
+    case VEGAS_ERR_DEVICE_FAULT: return "VEGAS_ERR_DEVICE_FAULT";
+    case VEGAS_ERR_DEVICE_TIMEOUT: return "VEGAS_ERR_DEVICE_TIMEOUT";
+  }
+  return "VEGAS_ERR_UNKNOWN";
+}
+
+VEGAS_API const char* vegas_last_error_detail(void) { return g_detail; }
+
+VEGAS_API int vegas_abi_version(void) { return VEGAS_ABI_VERSION; }

@@ -8,3 +8,14 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs on the GB300 box)")
+
+
+def pytest_sessionstart(session):
+    # On a GPU machine make sure the CUDA library exists before GPU tests import it.
+    try:
+        import torch
+    except ImportError:
+        return
+    if torch.cuda.is_available():
+        from self_speculative_sparse_paged_gb300 import _build
+        _build.build()

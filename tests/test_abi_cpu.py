@@ -1,0 +1,81 @@
+"""The C-ABI library loads and exports every declared entry point (no GPU needed).
+
+Only host-side argument validation is exercised here: those calls return a
+status before anything touches a device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def vg():
+    from self_speculative_sparse_paged_gb300 import _build
+    try:
+        _build.build()
+    except RuntimeError as e:          # no nvcc on this machine
+        pytest.skip(str(e))
+    import self_speculative_sparse_paged_gb300 as mod
+    return mod
+
+
+def _declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(vegas_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(vg):
+    decl = _declared_functions()
+    assert "vegas_verify_attn_capture" in decl and "vegas_select_topk" in decl
+    assert "vegas_sparse_decode_attn" in decl
+    lib = ctypes.CDLL(vg.library_path())
+    for name in decl:
+        assert hasattr(lib, name), name
+
+
+def test_binding_uses_the_same_names(vg):
+    for name in _declared_functions():
+        assert callable(getattr(vg, name)), name
+
+
+def test_status_strings(vg):
+    assert vg.vegas_abi_version() == 1
+    for code, name in vg.STATUS.items():
+        assert vg.vegas_status_string(code) == name
+
+
+def test_host_validation_rejects_before_launch(vg):
+    kv = vg.PagedKV(0, 0, 0, 1, 16, 8, 2, 64, 1)        # NULL caches
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_capture(kv, 16, 16, None, 0, 16, 1, 4, 0, 4, 0.125, None, 0,
+                                     stream=0)
+    assert ei.value.status == 1
+    kv = vg.PagedKV(16, 16, 16, 1, 8, 8, 2, 64, 1)      # page size 8
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_capture(kv, 16, 16, None, 0, 16, 1, 4, 0, 4, 0.125, None, 0,
+                                     stream=0)
+    assert ei.value.status == 2
+    kv = vg.PagedKV(16, 16, 16, 1, 16, 8, 2, 96, 1)     # head_dim 96
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_sparse_decode_attn(kv, 16, 16, 16, 4, 16, 16, 16, 1, 1, 0.1, None, 0, stream=0)
+    assert ei.value.status == 2
+    kv = vg.PagedKV(16, 16, 16, 1, 16, 64, 2, 128, 1)   # (gamma+1)*G = 5*32 rows
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_capture(kv, 16, 16, None, 0, 16, 1, 4, 0, 4, 0.125, None, 0,
+                                     stream=0)
+    assert ei.value.status == 2
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_select_topk(None, 16, 16, 16, 16, 1, 8, 10, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_select_topk(16, 16 * 32768 + 1, 16, 16, 16, 1, 8, 10, stream=0)
+    assert ei.value.status == 2

@@ -1,0 +1,58 @@
+"""Top-k select on the GPU: bit-exact against the oracle on identical fp32 scores."""
+import numpy as np
+import pytest
+import torch
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import oracle  # noqa: E402
+import self_speculative_sparse_paged_gb300 as vg  # noqa: E402
+from vegas_case import DEV, to_dev  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(scores32: np.ndarray, lens, kps, k_max, stride=None):
+    B, H, S = scores32.shape
+    idx = torch.full((B, H, k_max), -7, dtype=torch.int32, device=DEV)
+    vg.vegas_select_topk(to_dev(scores32), S, to_dev(np.asarray(lens, np.int32)),
+                         to_dev(np.asarray(kps, np.int32)), idx, B, H, k_max)
+    vg.vegas_read_device_status()
+    got = idx.cpu().numpy()
+    ref = oracle.select_topk_batch(scores32.astype(np.float64), np.asarray(lens),
+                                   np.asarray(kps), k_max)
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("L,k", [(1, 1), (5, 2), (1000, 0), (1000, 1000), (1000, 37),
+                                 (4097, 205), (32768, 1639), (65536, 3277), (131072, 3933),
+                                 (262144, 5000)])
+def test_select_random_scores(L, k):
+    rng = np.random.default_rng(L + k)
+    s = (rng.standard_normal((2, 3, L)) * 3).astype(np.float32)
+    _run(s, [L, L], [k, k], max(k, 1) + 3)
+
+
+def test_select_heavy_ties_and_signed_zero():
+    rng = np.random.default_rng(1)
+    s = rng.integers(-3, 3, size=(1, 4, 50000)).astype(np.float32)
+    s[0, 1, ::2] = -0.0
+    s[0, 1, 1::2] = 0.0
+    s[0, 2, :] = 1.5
+    _run(s, [50000], [777], 800)
+
+
+def test_select_variable_lengths_and_k():
+    rng = np.random.default_rng(2)
+    lens = [10, 40000, 3, 20001]
+    kps = [10, 2000, 0, 1]
+    s = (rng.standard_normal((4, 2, 40000)) * 10).astype(np.float32)
+    _run(s, lens, kps, 2100)
+
+
+def test_select_clustered_values():
+    """Scores concentrated in a few float exponent bins (the radix worst case)."""
+    rng = np.random.default_rng(3)
+    s = (1000.0 + rng.integers(0, 64, size=(1, 8, 32768)) * 2.0 ** -10).astype(np.float32)
+    _run(s, [32768], [1639], 1639)

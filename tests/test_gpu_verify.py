@@ -1,0 +1,84 @@
+"""Verify attention + Collect-2-Query capture on the GPU against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import oracle  # noqa: E402
+from vegas_case import Case, assert_attention_close, bf16_to_f64, score_bound  # noqa: E402
+from workload import configs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+T, C2, C3, C4 = (configs.TINY, configs.QWEN3_8B_B1_32K, configs.QWEN3_8B_B8_48K_64K,
+                 configs.GPTOSS_20B_B4_128K)
+
+SMALL = {
+    "tiny": T,
+    "qwen_b1_ragged": C2.with_(ctx_lo=3001, ctx_hi=3001),
+    "qwen_b3_var": C3.with_(batch=3, ctx_lo=900, ctx_hi=2100),
+    "gptoss_b2": C4.with_(batch=2, ctx_lo=2500, ctx_hi=2500),
+    "gamma0": C2.with_(gamma=0, ctx_lo=37, ctx_hi=37),
+    "len1": T.with_(ctx_lo=1, ctx_hi=1, k_abs=1),
+    "len0": T.with_(ctx_lo=0, ctx_hi=0, k_abs=0),
+    "qwen_gamma8": C2.with_(gamma=8, ctx_lo=1500, ctx_hi=1500),     # 36 rows, Q in smem
+    "qwen_gamma11": C2.with_(gamma=11, ctx_lo=700, ctx_hi=700),     # 48 rows
+    "gptoss_gamma7": C4.with_(batch=1, gamma=7, ctx_lo=900, ctx_hi=900),  # 64 rows
+    "mha_g1": T.with_(hq=4, hkv=4, gamma=3, ctx_lo=600, ctx_hi=600),
+    "long_split": C2.with_(ctx_lo=20000, ctx_hi=20000, hkv=2, hq=8),
+}
+
+
+def _check_case(c: Case, rows=None, capture=True):
+    out, scores = c.verify(capture=capture, rows=rows)
+    kf, vf = c.caches_f64()
+    qv = c.qv_f64()
+    ref_o = oracle.verify_attention(qv, kf, vf, c.pm.block_table, c.lens, c.scale)
+    assert_attention_close(bf16_to_f64(out), ref_o, "verify output")
+    if not capture:
+        return out, None
+    rows = rows if rows is not None else (0, c.w.gamma)
+    ref_s = oracle.capture_scores(qv, kf, c.pm.block_table, c.lens, c.scale,
+                                  rows=sorted(set(rows)))
+    got = scores.cpu().numpy().astype(np.float64)
+    G = c.w.group
+    for b in range(c.w.batch):
+        L = int(c.lens[b])
+        for g in range(c.w.hkv):
+            if L == 0:
+                continue
+            K = oracle.gather_rows(kf, c.pm.block_table[b], g, np.arange(L))
+            qr = np.concatenate([qv[b, t, g * G:(g + 1) * G] for t in sorted(set(rows))])
+            bound = score_bound(qr, K, c.scale) + 1e-30
+            err = np.abs(got[b, g, :L] - ref_s[b, g, :L])
+            assert np.all(err <= bound), f"score error {err.max()} > bound (b={b}, g={g})"
+            # positions past L_b are never written
+            assert np.all(np.isnan(got[b, g, L:])), "score written past the prefix"
+    return out, scores
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_verify_capture_matches_oracle(name):
+    _check_case(Case(SMALL[name]))
+
+
+def test_capture_switch_leaves_output_bit_identical():
+    c = Case(SMALL["qwen_b3_var"])
+    o1, _ = c.verify(capture=True)
+    o2, _ = c.verify(capture=False)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+@pytest.mark.parametrize("rows", [(0, 0), (1, 4), (4, 4), (2, 3)])
+def test_capture_row_choice(rows):
+    _check_case(Case(T), rows=rows)
+
+
+def test_repeat_calls_are_deterministic():
+    c = Case(SMALL["gptoss_b2"])
+    o1, s1 = c.verify()
+    o2, s2 = c.verify()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(s1, s2)
