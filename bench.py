@@ -1,0 +1,480 @@
+"""Benchmark of the Vegas hot path on GB300: one step = one iteration
+(verify + Collect-2-Query capture, top-k select, gamma sparse draft steps) of
+the Qwen3-8B-shaped layer at batch 1, context 32768, gamma 4, k = 5%.
+
+Prints one JSON line.  `value` is algorithmic HBM GB/s of the whole iteration
+(K/V rows the method must read, captured scores written and read, queries,
+outputs and indices) divided by the device time per iteration; `ms_per_step`
+is that time.  Inputs are resident in HBM; successive steps rotate over four
+copies of the paged cache (>4x the 129 MB L2) so no step finds its K/V in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation:
+the source pages publish no code) on the host cores, on a bounded sample.
+Under torchrun each rank runs its own replica of the workload (weak scaling).
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle legs run single-threaded BLAS so that `cores` is exact.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workload import configs, gen  # noqa: E402
+
+METRIC = ("µs and HBM GB/s (% of 8 TB/s) per verify+select+γ-draft iteration at "
+          "32K–128K")
+WORKLOAD = configs.QWEN3_8B_B1_32K
+ROOFLINE_TBS = 8.0
+REPLICAS = 4
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w, lens, kps):
+    """Bytes one iteration must move, by stage."""
+    d, hkv, hq, T = w.head_dim, w.hkv, w.hq, w.gamma + 1
+    row = 4 * d                                   # K + V bf16 per (position, KV head)
+    L = np.asarray(lens, dtype=np.int64)
+    k = np.asarray(kps, dtype=np.int64)
+    verify = int(hkv * row * (L + T).sum() + 2 * 2 * d * hq * T * len(L) + 4 * hkv * L.sum())
+    select = int(4 * hkv * L.sum() + 4 * hkv * k.sum())
+    draft = [int(hkv * row * (k + w.gamma + 2 + j).sum() + 4 * hkv * k.sum() + 2 * 2 * d * hq * len(L))
+             for j in range(w.gamma)]
+    return {"verify": verify, "select": select, "draft": draft,
+            "total": verify + select + sum(draft)}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class GpuIteration:
+    """The workload resident in HBM: REPLICAS copies of the paged cache in one
+    pool (replica r uses physical pages [r * P, (r + 1) * P)), shared queries,
+    outputs and workspaces."""
+
+    def __init__(self, w, replicas, dev):
+        import torch
+        import self_speculative_sparse_paged_gb300 as vg
+        self.torch, self.vg, self.w, self.dev, self.R = torch, vg, w, dev, replicas
+        self.lens = gen.ctx_lens(w)
+        self.kps = gen.k_per_seq(w, self.lens)
+        pm = gen.page_map(w, self.lens)
+        self.pm = pm
+        P = pm.num_pages
+        shape = (replicas * P, w.hkv, 16, w.head_dim)
+        self.k = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        self.v = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        lens_t = t(self.lens)
+        need = t(gen.positions_needed(w, self.lens).astype(np.int32))
+        u = t(gen.unit_direction(w))
+        owner = t(pm.owner)
+        for which, buf in ((0, self.k), (1, self.v)):
+            vg.vegas_synth_paged_kv(buf, which, w.seed, 0, owner, P, w.hkv, w.head_dim,
+                                    pm.max_pages, lens_t, need, gen.heavy_threshold(w),
+                                    w.heavy_last, u)
+        for r in range(1, replicas):
+            self.k[r * P:(r + 1) * P].copy_(self.k[:P])
+            self.v[r * P:(r + 1) * P].copy_(self.v[:P])
+        bt = pm.block_table
+        self.bt = t(np.stack([np.where(bt >= 0, bt + r * P, -1).astype(np.int32)
+                              for r in range(replicas)]))
+        self.kv = [vg.paged_kv(self.k, self.v, self.bt[r], w.hq) for r in range(replicas)]
+        bf = lambda a: t(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+        self.qv = bf(gen.f32_to_bf16_bits(gen.verify_queries_f32(w)))
+        self.qd = bf(gen.f32_to_bf16_bits(gen.draft_queries_f32(w)))
+        self.lens_t, self.kps_t = lens_t, t(self.kps)
+        self.stride = int(self.lens.max())
+        self.k_max = int(self.kps.max())
+        self.tails = [gen.tail_len(w, j) for j in range(w.gamma)]
+        self.tl_t = [torch.full((w.batch,), tl, dtype=torch.int32, device=dev) for tl in self.tails]
+        self.out_v = torch.empty_like(self.qv)
+        self.out_d = torch.empty_like(self.qd)
+        self.scores = torch.empty((w.batch, w.hkv, self.stride), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((w.batch, w.hkv, self.k_max), dtype=torch.int32, device=dev)
+        nv = vg.vegas_verify_workspace_size(self.kv[0], w.batch, w.gamma)
+        ns = vg.vegas_sparse_workspace_size(self.kv[0], w.batch, self.k_max, max(self.tails))
+        self.ws_v = torch.zeros(max(nv, 256), dtype=torch.uint8, device=dev)
+        self.ws_s = torch.zeros(max(ns, 256), dtype=torch.uint8, device=dev)
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        self.launches_per_step = 2 + w.gamma
+
+    def verify(self, r, capture=True):
+        w = self.w
+        self.vg.vegas_verify_attn_capture(
+            self.kv[r], self.qv, self.out_v, self.scores if capture else None, self.stride,
+            self.lens_t, w.batch, w.gamma, 0, w.gamma, self.scale, self.ws_v, self.ws_v.numel())
+
+    def select(self):
+        w = self.w
+        self.vg.vegas_select_topk(self.scores, self.stride, self.lens_t, self.kps_t, self.idx,
+                                  w.batch, w.hkv, self.k_max)
+
+    def draft(self, r, j):
+        w = self.w
+        self.vg.vegas_sparse_decode_attn(
+            self.kv[r], self.qd[j], self.out_d[j], self.idx, self.k_max, self.kps_t, self.lens_t,
+            self.tl_t[j], self.tails[j], w.batch, self.scale, self.ws_s, self.ws_s.numel())
+
+    def step(self, r, ev=None):
+        if ev:
+            ev[0].record()
+        self.verify(r)
+        if ev:
+            ev[1].record()
+        self.select()
+        if ev:
+            ev[2].record()
+        for j in range(self.w.gamma):
+            self.draft(r, j)
+        if ev:
+            ev[3].record()
+
+
+def make_events(torch, n, external):
+    if external:
+        return [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+                for _ in range(n)]
+    return None
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    it = GpuIteration(w, REPLICAS, dev)
+    vg = it.vg
+    nbytes = algorithmic_bytes(w, it.lens, it.kps)
+    stream = torch.cuda.Stream(device=dev)
+    K, W = args.steps, args.warmup
+
+    # warm-up: every path once eagerly (configures kernels), then W steps
+    with torch.cuda.stream(stream):
+        for i in range(max(W, 1)):
+            it.step(i % REPLICAS)
+            it.verify(i % REPLICAS, capture=False)
+    stream.synchronize()
+    vg.vegas_read_device_status(stream)
+
+    chunk = max(REPLICAS, min(K, 100) // REPLICAS * REPLICAS)
+    reps = max(1, math.ceil(K / chunk))
+    K_eff = reps * chunk
+    try:
+        evs = make_events(torch, chunk, True)
+    except TypeError:
+        evs = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(chunk):
+            it.step(i % REPLICAS, evs[i] if evs else None)
+    plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(plain, stream=stream):
+        for i in range(chunk):
+            it.verify(i % REPLICAS, capture=False)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        plain.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record()
+        for _ in range(reps):
+            graph.replay()
+        t1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    # plain verify (capture compiled out), same rotation, for the capture overhead
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        p0.record()
+        for _ in range(max(1, reps // 2)):
+            plain.replay()
+        p1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    vg.vegas_read_device_status(stream)
+    verify_plain_us = 1000.0 * p0.elapsed_time(p1) / (max(1, reps // 2) * chunk)
+
+    if dist:
+        tm = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms_total = float(tm.item())
+    ms_step = ms_total / K_eff
+
+    stages = None
+    if evs:
+        v = [evs[i][0].elapsed_time(evs[i][1]) for i in range(chunk)]
+        s = [evs[i][1].elapsed_time(evs[i][2]) for i in range(chunk)]
+        d = [evs[i][2].elapsed_time(evs[i][3]) for i in range(chunk)]
+        stages = {"verify_us": 1000 * statistics.mean(v), "select_us": 1000 * statistics.mean(s),
+                  "draft_us_per_step": 1000 * statistics.mean(d) / w.gamma,
+                  "source": "external CUDA events in the replayed graph (last replay)"}
+    e2e = run_e2e(it, stream, min(K_eff, 500), nbytes)
+    return it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e
+
+
+def run_e2e(it, stream, steps, nbytes):
+    """Same metric through the public API with host buffers: every step copies
+    its queries from pinned host memory, runs the iteration, and reads back the
+    verify outputs, the draft outputs and the selected indices."""
+    torch = it.torch
+    pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)  # noqa: E731
+    qv_h, qd_h = pin(it.qv), pin(it.qd)
+    qv_h.copy_(it.qv.cpu())
+    qd_h.copy_(it.qd.cpu())
+    ov_h, od_h, idx_h = pin(it.out_v), pin(it.out_d), pin(it.idx)
+    graphs = []
+    for r in range(it.R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            it.step(r)
+        graphs.append(g)
+    bi = qv_h.numel() * 2 + qd_h.numel() * 2
+    bo = ov_h.numel() * 2 + od_h.numel() * 2 + idx_h.numel() * 4
+
+    def one(i):
+        with torch.cuda.stream(stream):
+            it.qv.copy_(qv_h, non_blocking=True)
+            it.qd.copy_(qd_h, non_blocking=True)
+            graphs[i % it.R].replay()
+            ov_h.copy_(it.out_v, non_blocking=True)
+            od_h.copy_(it.out_d, non_blocking=True)
+            idx_h.copy_(it.idx, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(nbytes["total"] / dt / 1e9, 2), "unit": "GB/s",
+            "us_per_iteration": round(dt * 1e6, 2), "steps": steps,
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+            "timing": "host wall clock, stream synchronised every step"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+class OracleWorkload:
+    """Host fp64 inputs of the workload for the oracle."""
+
+    def __init__(self, w):
+        self.w = w
+        self.lens = gen.ctx_lens(w)
+        self.kps = gen.k_per_seq(w, self.lens)
+        self.pm = gen.page_map(w, self.lens)
+        self.kf = gen.bf16_bits_to_f64(gen.paged_cache_bf16(w, 0, "k", self.lens, self.pm))
+        self.vf = gen.bf16_bits_to_f64(gen.paged_cache_bf16(w, 0, "v", self.lens, self.pm))
+        self.qv = gen.bf16_bits_to_f64(gen.f32_to_bf16_bits(gen.verify_queries_f32(w)))
+        self.qd = gen.bf16_bits_to_f64(gen.f32_to_bf16_bits(gen.draft_queries_f32(w)))
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+
+    def unit_step(self, g):
+        """The oracle iteration restricted to KV head g of every sequence."""
+        import oracle
+        w, G = self.w, self.w.group
+        heads = slice(g * G, (g + 1) * G)
+        sub_k = self.kf[:, g:g + 1]
+        sub_v = self.vf[:, g:g + 1]
+        oracle.iteration(self.qv[:, :, heads], self.qd[:, :, heads], sub_k, sub_v,
+                         self.pm.block_table, self.lens, self.kps, self.scale)
+
+
+def time_oracle(w, nbytes, budget_s, min_steps=1, max_steps=None):
+    """Times oracle unit steps (one KV head each) until budget_s or max_steps."""
+    ow = OracleWorkload(w)
+    per_unit = nbytes["total"] / w.hkv
+    ow.unit_step(0)                      # warm-up (imports, caches)
+    times = []
+    t_start = time.perf_counter()
+    i = 0
+    while True:
+        t0 = time.perf_counter()
+        ow.unit_step(i % w.hkv)
+        times.append(time.perf_counter() - t0)
+        i += 1
+        if max_steps is not None and i >= max_steps:
+            break
+        if i >= min_steps and time.perf_counter() - t_start >= budget_s:
+            break
+    dt = statistics.mean(times)
+    return {"value": round(per_unit / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "steps": len(times), "s_per_unit_step": round(dt, 3),
+            "sample": (f"{len(times)} oracle steps, each one full iteration of the workload "
+                       f"restricted to one of its {w.hkv} KV heads (fp64 numpy, one thread)")}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def base_config(w, lens, kps):
+    return {"workload": w.name, "description": w.description, "batch": w.batch,
+            "ctx_len": int(lens.max()), "gamma": w.gamma, "k": int(kps.max()),
+            "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim, "page_size": 16,
+            "l2": f"steps rotate over {REPLICAS} copies of the paged KV cache "
+                  f"({REPLICAS}x {w.hkv * 4 * w.head_dim * int(lens.max()) / 1e6:.0f} MB)",
+            "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = WORKLOAD
+    lens, kps = gen.ctx_lens(w), gen.k_per_seq(w, gen.ctx_lens(w))
+    nbytes = algorithmic_bytes(w, lens, kps)
+    peak, peak_kind = read_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ref = time_oracle(w, nbytes, budget_s=150.0, min_steps=args.steps + args.warmup,
+                          max_steps=args.steps + args.warmup)
+        gbs = ref["value"]
+        us = nbytes["total"] / (gbs * 1e9) * 1e6
+        line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": ref["steps"], "warmup": 0,
+                "ms_per_step": round(us / 1000, 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": base_config(w, lens, kps),
+                "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "note": "fp64 CPU oracle; the pages publish no implementation to install"}
+        print(json.dumps(line))
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e = run_gpu(args, rank, world,
+                                                                              dist)
+    us_step = ms_step * 1000.0
+    gbs = nbytes["total"] / (us_step * 1e-6) / 1e9
+    line = {"metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s",
+            "n_gpus": world, "steps": K_eff, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 5), "us_per_iteration": round(us_step, 2),
+            "pct_of_8tbs": round(100 * gbs / (ROOFLINE_TBS * 1000), 2),
+            "pct_of_measured_hbm": round(100 * gbs / peak, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": base_config(it.w, it.lens, it.kps),
+            "bytes_per_iteration": nbytes["total"],
+            "gpu_launches": K_eff * it.launches_per_step, "clocks": clocks, "e2e": e2e}
+    if stages:
+        v_us = stages["verify_us"]
+        line["stages"] = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in stages.items()}
+        line["stages"]["verify_plain_us"] = round(verify_plain_us, 3)
+        line["capture_plus_select_overhead"] = round(
+            (v_us + stages["select_us"]) / verify_plain_us - 1.0, 4)
+        achieved = nbytes["verify"] / (v_us * 1e-6) / 1e9
+        line["roofline"] = {"kernel": "verify_attn_kernel", "bound": "hbm",
+                            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                            "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                            "traffic": None,
+                            "bytes_per_launch": nbytes["verify"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ref = time_oracle(it.w, nbytes, budget_s=15.0)
+        line["cpu_baseline"] = {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
