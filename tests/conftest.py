@@ -17,5 +17,5 @@ def pytest_sessionstart(session):
     except ImportError:
         return
     if torch.cuda.is_available():
-        from self_speculative_sparse_paged_gb300 import _build
-        _build.build()
+        import __graft_entry__
+        __graft_entry__.build()

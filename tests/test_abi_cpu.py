@@ -14,9 +14,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def vg():
-    from self_speculative_sparse_paged_gb300 import _build
+    import __graft_entry__
     try:
-        _build.build()
+        __graft_entry__.build()
     except RuntimeError as e:          # no nvcc on this machine
         pytest.skip(str(e))
     import self_speculative_sparse_paged_gb300 as mod
