@@ -187,10 +187,10 @@ class GpuIteration:
             self.kv[r], self.qd[j], self.out_d[j], self.idx, self.k_max, self.kps_t, self.lens_t,
             self.tl_t[j], self.tails[j], w.batch, self.scale, self.ws_s, self.ws_s.numel())
 
-    def step(self, r, ev=None):
+    def step(self, r, ev=None, capture=True):
         if ev:
             ev[0].record()
-        self.verify(r)
+        self.verify(r, capture)
         if ev:
             ev[1].record()
         self.select()
@@ -239,10 +239,13 @@ def run_gpu(args, rank, world, dist):
     with torch.cuda.graph(graph, stream=stream):
         for i in range(chunk):
             it.step(i % REPLICAS, evs[i] if evs else None)
+    # the same iteration with the capture compiled out of verify (select then
+    # reads the previous scores): the denominator of the capture overhead
+    evp = make_events(torch, chunk, True) if evs else None
     plain = torch.cuda.CUDAGraph()
     with torch.cuda.graph(plain, stream=stream):
         for i in range(chunk):
-            it.verify(i % REPLICAS, capture=False)
+            it.step(i % REPLICAS, evp[i] if evp else None, capture=False)
     with torch.cuda.stream(stream):
         graph.replay()
         plain.replay()
@@ -276,7 +279,11 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.synchronize()
     clocks = sampler.stop()
     vg.vegas_read_device_status(stream)
-    verify_plain_us = 1000.0 * p0.elapsed_time(p1) / (max(1, reps // 2) * chunk)
+    if evp:
+        verify_plain_us = 1000 * statistics.mean(evp[i][0].elapsed_time(evp[i][1])
+                                                 for i in range(chunk))
+    else:
+        verify_plain_us = float("nan")
 
     if dist:
         tm = torch.tensor([ms_total], dtype=torch.float64, device=dev)

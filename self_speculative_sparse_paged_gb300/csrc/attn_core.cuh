@@ -26,6 +26,9 @@
 namespace vegas {
 
 constexpr float kRescaleSlack = 8.0f;
+// Running max of a column that has seen no logit yet (finite, so that
+// 2^(x - m) and 2^(m_old - m_new) never form inf - inf).
+constexpr float kEmptyMax = -1.0e30f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // 16-row tile written by a 2-D TMA load with 128-byte swizzle: D/64 boxes of
@@ -63,7 +66,7 @@ struct WarpState {
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        m[nt][e] = -INFINITY;
+        m[nt][e] = kEmptyMax;
         l[nt][e] = 0.f;
       }
   }
@@ -86,83 +89,111 @@ __device__ __forceinline__ void load_q_frags(uint32_t q_base, uint32_t (&qf)[D /
     }
 }
 
-// S^T for one 16-position tile.
-template <int D, int NT, class Tile>
-__device__ __forceinline__ void tile_scores(uint32_t k_base, const uint32_t (&qf)[D / 16][NT][2],
-                                            float (&s)[NT][4]) {
+// S^T for P 16-position tiles (one per page), the pages' MMA chains interleaved.
+template <int D, int NT, int P, class Tile>
+__device__ __forceinline__ void tile_scores(const uint32_t (&k_base)[P],
+                                            const uint32_t (&qf)[D / 16][NT][2],
+                                            float (&s)[P][NT][4]) {
   const int lane = threadIdx.x & 31;
   const int mi = lane >> 3;
   const int row = (lane & 7) + 8 * (mi & 1);
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int pg = 0; pg < P; ++pg)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[pg][nt][i] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    uint32_t a0, a1, a2, a3;
-    ldmatrix_x4(Tile::addr(k_base, row, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+    uint32_t a[P][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+    for (int pg = 0; pg < P; ++pg)
+      ldmatrix_x4(Tile::addr(k_base[pg], row, 2 * ks + (mi >> 1)), a[pg][0], a[pg][1], a[pg][2],
+                  a[pg][3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int pg = 0; pg < P; ++pg)
+        mma_bf16_16816(s[pg][nt], a[pg][0], a[pg][1], a[pg][2], a[pg][3], qf[ks][nt][0],
+                       qf[ks][nt][1]);
   }
 }
 
-// S^T for one 16-position tile, reading the Q^T fragments from the padded Q
-// tile in shared memory at every k-step (used where registers are short).
-template <int D, int NT, class Tile>
-__device__ __forceinline__ void tile_scores_qsmem(uint32_t k_base, uint32_t q_base,
-                                                  float (&s)[NT][4]) {
+// As tile_scores, reading the Q^T fragments from the padded Q tile in shared
+// memory at every k-step (used where registers are short).
+template <int D, int NT, int P, class Tile>
+__device__ __forceinline__ void tile_scores_qsmem(const uint32_t (&k_base)[P], uint32_t q_base,
+                                                  float (&s)[P][NT][4]) {
   const int lane = threadIdx.x & 31;
   const int mi = lane >> 3;
   const int row = (lane & 7) + 8 * (mi & 1);
   constexpr int kRow = D * 2 + 16;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int pg = 0; pg < P; ++pg)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[pg][nt][i] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    uint32_t a0, a1, a2, a3;
-    ldmatrix_x4(Tile::addr(k_base, row, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+    uint32_t a[P][4];
+#pragma unroll
+    for (int pg = 0; pg < P; ++pg)
+      ldmatrix_x4(Tile::addr(k_base[pg], row, 2 * ks + (mi >> 1)), a[pg][0], a[pg][1], a[pg][2],
+                  a[pg][3]);
 #pragma unroll
     for (int nt = 0; nt < NT; nt += 2) {
       if (nt + 1 < NT) {
         uint32_t b0, b1, b2, b3;
         const int qrow = (nt + (mi >> 1)) * 8 + (lane & 7);
         ldmatrix_x4(q_base + qrow * kRow + (2 * ks + (mi & 1)) * 16, b0, b1, b2, b3);
-        mma_bf16_16816(s[nt], a0, a1, a2, a3, b0, b1);
-        mma_bf16_16816(s[nt + 1], a0, a1, a2, a3, b2, b3);
+#pragma unroll
+        for (int pg = 0; pg < P; ++pg) {
+          mma_bf16_16816(s[pg][nt], a[pg][0], a[pg][1], a[pg][2], a[pg][3], b0, b1);
+          mma_bf16_16816(s[pg][nt + 1], a[pg][0], a[pg][1], a[pg][2], a[pg][3], b2, b3);
+        }
       } else {
         uint32_t b0, b1;
         const int qrow = nt * 8 + (lane & 7);
         ldmatrix_x2(q_base + qrow * kRow + (2 * ks + ((lane >> 3) & 1)) * 16, b0, b1);
-        mma_bf16_16816(s[nt], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+        for (int pg = 0; pg < P; ++pg)
+          mma_bf16_16816(s[pg][nt], a[pg][0], a[pg][1], a[pg][2], a[pg][3], b0, b1);
       }
     }
   }
 }
 
-// Online-softmax update with the tile's log2-unit logits x (masked entries
-// -inf), then O^T += V^T P^T.
-template <int D, int NT, class Tile>
-__device__ __forceinline__ void tile_softmax_pv(WarpState<D, NT>& st, const float (&x)[NT][4],
-                                                uint32_t v_base) {
+// Online-softmax update with the P tiles' log2-unit logits x (masked entries
+// -inf), then O^T += V^T P^T over the P pages.  The running max starts at a
+// finite kEmptyMax, so 2^(x - m) needs no guard: a masked x gives 0.
+template <int D, int NT, int P, class Tile>
+__device__ __forceinline__ void tile_softmax_pv(WarpState<D, NT>& st, const float (&x)[P][NT][4],
+                                                const uint32_t (&v_base)[P]) {
   const int lane = threadIdx.x & 31;
   bool need = false;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) need |= fmaxf(x[nt][e], x[nt][2 + e]) > st.m[nt][e] + kRescaleSlack;
+    for (int e = 0; e < 2; ++e) {
+      float mx = fmaxf(x[0][nt][e], x[0][nt][2 + e]);
+#pragma unroll
+      for (int pg = 1; pg < P; ++pg) mx = fmaxf(mx, fmaxf(x[pg][nt][e], x[pg][nt][2 + e]));
+      need |= mx > st.m[nt][e] + kRescaleSlack;
+    }
   if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float mx = fmaxf(x[nt][e], x[nt][2 + e]);
+        float mx = fmaxf(x[0][nt][e], x[0][nt][2 + e]);
+#pragma unroll
+        for (int pg = 1; pg < P; ++pg) mx = fmaxf(mx, fmaxf(x[pg][nt][e], x[pg][nt][2 + e]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(st.m[nt][e], mx);
-        const float alpha = (mnew == -INFINITY) ? 1.f : ex2(st.m[nt][e] - mnew);
+        const float alpha = ex2(st.m[nt][e] - mnew);
         st.m[nt][e] = mnew;
         st.l[nt][e] *= alpha;
 #pragma unroll
@@ -172,28 +203,31 @@ __device__ __forceinline__ void tile_softmax_pv(WarpState<D, NT>& st, const floa
         }
       }
   }
-  uint32_t pb[NT][2];
+  uint32_t pb[P][NT][2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    float p[4];
+  for (int pg = 0; pg < P; ++pg)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float xi = x[nt][i];
-      p[i] = (xi == -INFINITY) ? 0.f : ex2(xi - st.m[nt][i & 1]);
+    for (int nt = 0; nt < NT; ++nt) {
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = ex2(x[pg][nt][i] - st.m[nt][i & 1]);
+      st.l[nt][0] += p[0] + p[2];
+      st.l[nt][1] += p[1] + p[3];
+      pb[pg][nt][0] = movmatrix_trans(pack_bf16x2(p[0], p[1]));
+      pb[pg][nt][1] = movmatrix_trans(pack_bf16x2(p[2], p[3]));
     }
-    st.l[nt][0] += p[0] + p[2];
-    st.l[nt][1] += p[1] + p[3];
-    pb[nt][0] = movmatrix_trans(pack_bf16x2(p[0], p[1]));
-    pb[nt][1] = movmatrix_trans(pack_bf16x2(p[2], p[3]));
-  }
   const int mi = lane >> 3;
   const int prow = (lane & 7) + 8 * (mi >> 1);
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
-    uint32_t a0, a1, a2, a3;
-    ldmatrix_x4_trans(Tile::addr(v_base, prow, 2 * mt + (mi & 1)), a0, a1, a2, a3);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(st.o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+    for (int pg = 0; pg < P; ++pg) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4_trans(Tile::addr(v_base[pg], prow, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_bf16_16816(st.o[mt][nt], a0, a1, a2, a3, pb[pg][nt][0], pb[pg][nt][1]);
+    }
   }
 }
 

@@ -100,18 +100,38 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
   const int start = rank * p.chunk;
   const int cnt = max(0, min(L - start, p.chunk));
   const float* src = p.scores + size_t(unit) * p.score_stride + start;
-  for (int i = tid; i < cnt; i += kSelThreads) keys[i] = order_key(src[i]);
+  // Loads are issued in batches of 8 per thread before any of them is used.
+  for (int i0 = 0; i0 < cnt; i0 += 8 * kSelThreads) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSelThreads + tid;
+      v[u] = i < cnt ? __ldcg(&src[i]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSelThreads + tid;
+      if (i < cnt) keys[i] = order_key(v[u]);
+    }
+  }
 
   uint32_t prefix = 0u, pmask = 0u;
   uint32_t krem = (uint32_t)k;
+  const int lane = tid & 31;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     uint32_t* h = hist[pass & 1];
     if (tid < 256) h[tid] = 0u;
     __syncthreads();
-    for (int i = tid; i < cnt; i += kSelThreads) {
-      const uint32_t key = keys[i];
-      if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+    // Lanes holding the same digit add once per warp (match.any), which keeps
+    // the heavily shared top digits from serialising on one bank.
+    for (int i0 = 0; i0 < cnt; i0 += kSelThreads) {
+      const int i = i0 + tid;
+      const uint32_t key = i < cnt ? keys[i] : 0u;
+      const bool in = i < cnt && (key & pmask) == prefix;
+      const uint32_t digit = in ? ((key >> shift) & 255u) : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&h[digit], (uint32_t)__popc(peers));
     }
     cluster.sync();
     uint32_t v = 0u;

@@ -79,19 +79,36 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
     fence_mbar_init();
   }
   // Entry e of the list: T[e] for e < k_b, else tail_start + (e - k_b).
-  for (int i = tid; i < nrows; i += W * 32) {
-    const int e = rbeg + i;
-    int pos = e < kb ? p.idx[size_t(unit) * p.k_max + e] : tstart + (e - kb);
-    if (pos < 0 || pos >= cap) {
-      set_error(p.err, kErrDeviceFault);
-      pos = 0;
+  // Resolved in batches: every index load of a thread, then every page load.
+  constexpr int kPer = SparseCfg<D>::kMaxRowsPerSplit / (W * 32);
+  {
+    int pos[kPer], phys[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + u * W * 32;
+      const int e = rbeg + i;
+      pos[u] = 0;
+      if (i < nrows) pos[u] = e < kb ? __ldcg(&p.idx[size_t(unit) * p.k_max + e]) : tstart + (e - kb);
     }
-    int phys = p.block_table[size_t(b) * p.max_pages + (pos >> 4)];
-    if (phys < 0 || phys >= p.num_pages) {
-      set_error(p.err, kErrDeviceFault);
-      phys = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      if (pos[u] < 0 || pos[u] >= cap) {
+        set_error(p.err, kErrDeviceFault);
+        pos[u] = 0;
+      }
+      phys[u] = tid + u * W * 32 < nrows ? __ldg(&p.block_table[size_t(b) * p.max_pages + (pos[u] >> 4)]) : 0;
     }
-    rows[i] = (phys * p.hkv + g) * 16 + (pos & 15);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + u * W * 32;
+      if (i < nrows) {
+        if (phys[u] < 0 || phys[u] >= p.num_pages) {
+          set_error(p.err, kErrDeviceFault);
+          phys[u] = 0;
+        }
+        rows[i] = (phys[u] * p.hkv + g) * 16 + (pos[u] & 15);
+      }
+    }
   }
   for (int i = tid; i < NPAD * (D / 8); i += W * 32) {
     const int n = i / (D / 8), c = i % (D / 8);
@@ -144,19 +161,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
       break;
     }
     const int grp = warp + i * W;
-    const uint32_t kb_s = stage0 + s * STAGE;
-    float sc[NT][4];
-    tile_scores<D, NT, Tile>(kb_s, qf, sc);
-    float x[NT][4];
+    const uint32_t kb_s[1] = {stage0 + s * STAGE};
+    const uint32_t vb_s[1] = {stage0 + s * STAGE + TILE};
+    float sc[1][NT][4];
+    tile_scores<D, NT, 1, Tile>(kb_s, qf, sc);
+    float x[1][NT][4];
     const int valid = nrows - grp * 16;   // rows of this group inside the range
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int r = (lane >> 2) + 8 * (k >> 1);
-        x[nt][k] = r < valid ? sc[nt][k] * p.scale_log2 : -INFINITY;
+        const int n = nt * 8 + 2 * (lane & 3) + (k & 1);
+        x[0][nt][k] = (r < valid && n < p.group) ? sc[0][nt][k] * p.scale_log2 : -INFINITY;
       }
-    tile_softmax_pv<D, NT, Tile>(st, x, kb_s + TILE);
+    tile_softmax_pv<D, NT, 1, Tile>(st, x, vb_s);
     __syncwarp();
     if (i + STAGES < nmy) {
       fence_proxy_async_smem();

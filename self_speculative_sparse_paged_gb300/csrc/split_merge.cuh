@@ -32,8 +32,8 @@ __device__ __forceinline__ void merge_and_write(const WarpState<D, NT>& st, uint
   constexpr int NPAD = NT * 8;
   constexpr int OS = D + 4;
   constexpr int NTH = W * 32;
-  constexpr int E = NPAD * D / NTH;   // output elements owned per thread
-  static_assert((NPAD * D) % NTH == 0, "element split");
+  constexpr int E = (NPAD * D + NTH - 1) / NTH;   // output elements owned per thread
+  const int nel = nq * D;                          // element e = n * D + dim, n < nq
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
 
@@ -86,8 +86,9 @@ __device__ __forceinline__ void merge_and_write(const WarpState<D, NT>& st, uint
     for (int j = 0; j < E; ++j) {
       const int e = tid + j * NTH;
       const int n = e / D, dim = e % D;
-      for (int w = w0; w < min(W, w0 + C); ++w)
-        acc[j] += cm[w * NPAD + n] * cO[((w - w0) * NPAD + n) * OS + dim];
+      if (e < nel)
+        for (int w = w0; w < min(W, w0 + C); ++w)
+          acc[j] += cm[w * NPAD + n] * cO[((w - w0) * NPAD + n) * OS + dim];
     }
     __syncthreads();
   }
@@ -125,35 +126,71 @@ __device__ __forceinline__ void merge_and_write(const WarpState<D, NT>& st, uint
   if (!*flag) return;
   __threadfence();
 
-  // Last CTA of the unit: weights w[s][n] = f_s / l, then the weighted sum.
-  float* wS = cO;   // [num_splits][nq]
+  // Last CTA of the unit.  Every split's (m, l) is staged in shared memory by
+  // one parallel sweep and turned into weights w[s][n] = f_s / l; the partial
+  // outputs are then summed with loads issued in independent batches.
+  float* wS = cO;                          // [num_splits][nq]
+  float* mS = wS + num_splits * nq;        // [num_splits][nq]
+  float* lS = mS + num_splits * nq;        // [num_splits][nq]
   const size_t base = (size_t)unit * num_splits;
+  const float2* ml = reinterpret_cast<const float2*>(ws.part_ml) + base * nq;
+  for (int i = tid; i < num_splits * nq; i += NTH) {
+    const float2 v = __ldcg(&ml[i]);
+    mS[i] = v.x;
+    lS[i] = v.y;
+  }
+  __syncthreads();
   for (int n = tid; n < nq; n += NTH) {
     float M = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) M = fmaxf(M, __ldcg(&ws.part_ml[((base + s) * nq + n) * 2]));
+    for (int s = 0; s < num_splits; ++s) M = fmaxf(M, mS[s * nq + n]);
     float L = 0.f;
     for (int s = 0; s < num_splits; ++s) {
-      const float ms = __ldcg(&ws.part_ml[((base + s) * nq + n) * 2]);
+      const float ms = mS[s * nq + n];
       const float f = (ms == -INFINITY) ? 0.f : ex2(ms - M);
       wS[s * nq + n] = f;
-      L += f * __ldcg(&ws.part_ml[((base + s) * nq + n) * 2 + 1]);
+      L += f * lS[s * nq + n];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int s = 0; s < num_splits; ++s) wS[s * nq + n] *= inv;
   }
   __syncthreads();
+  // Every split wrote a partial O (zeros where it attended nothing), so the
+  // weighted sum needs no branch.  Element e = n * D + dim of split s sits at
+  // part_o[(base + s) * nq * D + e].
+  const float* po = ws.part_o + base * nq * D;
+  float a[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) a[j] = 0.f;
+  constexpr int U = 4;
+  int s = 0;
+  for (; s + U <= num_splits; s += U) {
+    float v[U][E];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const int e = tid + j * NTH;
+        v[u][j] = e < nel ? __ldcg(&po[size_t(s + u) * nel + e]) : 0.f;
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const int n = min((tid + j * NTH) / D, nq - 1);
+        a[j] += wS[(s + u) * nq + n] * v[u][j];
+      }
+  }
+  for (; s < num_splits; ++s) {
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int e = tid + j * NTH;
+      if (e < nel) a[j] += wS[s * nq + e / D] * __ldcg(&po[size_t(s) * nel + e]);
+    }
+  }
 #pragma unroll
   for (int j = 0; j < E; ++j) {
     const int e = tid + j * NTH;
-    const int n = e / D, dim = e % D;
-    if (n < nq) {
-      float a = 0.f;
-      for (int s = 0; s < num_splits; ++s) {
-        const float w = wS[s * nq + n];
-        if (w != 0.f) a += w * __ldcg(&ws.part_o[((base + s) * nq + n) * D + dim]);
-      }
-      out_row(n)[dim] = __float2bfloat16_rn(a);
-    }
+    if (e < nel) out_row(e / D)[e % D] = __float2bfloat16_rn(a[j]);
   }
   if (tid == 0) ws.tickets[unit] = 0;
 }

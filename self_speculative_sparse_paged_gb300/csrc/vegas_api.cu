@@ -160,14 +160,20 @@ struct VerifyPlan {
   size_t tickets_off, ml_off, o_off, bytes;
 };
 
-VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms) {
+// Query columns of the verify tile: the (gamma+1)*G rows, plus with capture
+// two columns holding the summed captured query (at the next even index).
+int verify_columns(int nq, bool capture) { return capture ? ((nq + 1) & ~1) + 2 : nq; }
+
+VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms,
+                       bool capture = true) {
   VerifyPlan pl{};
   const int G = kv->num_q_heads / kv->num_kv_heads;
   pl.nq = (gamma + 1) * G;
-  pl.ntiles = (pl.nq + 7) / 8;
+  pl.ntiles = (verify_columns(pl.nq, capture) + 7) / 8;
   const int units = std::max(1, batch * kv->num_kv_heads);
   pl.splits = verify_splits(units, kv->max_pages_per_seq, sms);
   pl.pages_per_split = (kv->max_pages_per_seq + pl.splits - 1) / pl.splits;
+  pl.pages_per_split += pl.pages_per_split & 1;   // kernels step over page pairs
   pl.splits = (kv->max_pages_per_seq + pl.pages_per_split - 1) / pl.pages_per_split;
   pl.tickets_off = 0;
   pl.ml_off = align256(size_t(units) * 4);
@@ -235,8 +241,10 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   if (!std::isfinite(softmax_scale)) return fail(VEGAS_ERR_INVALID_ARG, "softmax_scale not finite");
   const int G = kv->num_q_heads / kv->num_kv_heads;
   const int nq = (gamma + 1) * G;
-  if ((nq + 7) / 8 > vegas::verify_max_ntiles(kv->head_dim))
-    return fail(VEGAS_ERR_UNSUPPORTED, "(gamma+1)*G = %d query rows exceeds %d for head_dim %d", nq,
+  const int ncols = verify_columns(nq, scores != nullptr);
+  if ((ncols + 7) / 8 > vegas::verify_max_ntiles(kv->head_dim))
+    return fail(VEGAS_ERR_UNSUPPORTED,
+                "(gamma+1)*G = %d query rows (+2 capture columns) exceeds %d for head_dim %d", nq,
                 8 * vegas::verify_max_ntiles(kv->head_dim), kv->head_dim);
   if (scores) {
     if (score_stride < 1) return fail(VEGAS_ERR_INVALID_ARG, "score_stride %d", score_stride);
@@ -248,7 +256,7 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   int* err = nullptr;
   int sms = 0;
   if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
-  const VerifyPlan pl = plan_verify(kv, batch, gamma, sms);
+  const VerifyPlan pl = plan_verify(kv, batch, gamma, sms, scores != nullptr);
   if (pl.splits > 1) {
     if (!workspace || workspace_bytes < pl.bytes)
       return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "verify workspace %zu < %zu bytes",

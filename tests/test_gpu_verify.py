@@ -24,9 +24,10 @@ SMALL = {
     "len1": T.with_(ctx_lo=1, ctx_hi=1, k_abs=1),
     "len0": T.with_(ctx_lo=0, ctx_hi=0, k_abs=0),
     "qwen_gamma8": C2.with_(gamma=8, ctx_lo=1500, ctx_hi=1500),     # 36 rows, Q in smem
-    "qwen_gamma11": C2.with_(gamma=11, ctx_lo=700, ctx_hi=700),     # 48 rows
-    "gptoss_gamma7": C4.with_(batch=1, gamma=7, ctx_lo=900, ctx_hi=900),  # 64 rows
+    "qwen_gamma10": C2.with_(gamma=10, ctx_lo=700, ctx_hi=700),     # 44 rows + 2 capture
+    "gptoss_gamma6_g9": C4.with_(batch=1, hq=72, hkv=8, gamma=5, ctx_lo=900, ctx_hi=900),  # 54 rows
     "mha_g1": T.with_(hq=4, hkv=4, gamma=3, ctx_lo=600, ctx_hi=600),
+    "odd_rows_g3": C4.with_(batch=1, hq=24, hkv=8, gamma=4, ctx_lo=500, ctx_hi=500),
     "long_split": C2.with_(ctx_lo=20000, ctx_hi=20000, hkv=2, hq=8),
 }
 
@@ -62,6 +63,14 @@ def _check_case(c: Case, rows=None, capture=True):
 @pytest.mark.parametrize("name", list(SMALL))
 def test_verify_capture_matches_oracle(name):
     _check_case(Case(SMALL[name]))
+
+
+@pytest.mark.parametrize("w", [C2.with_(gamma=11, ctx_lo=700, ctx_hi=700),
+                               C4.with_(batch=1, gamma=7, ctx_lo=900, ctx_hi=900)],
+                         ids=["qwen_48rows", "gptoss_64rows"])
+def test_verify_without_capture_at_the_row_limit(w):
+    """(gamma+1)*G at the tile limit (48 rows at d=128, 64 at d=64) without capture."""
+    _check_case(Case(w), capture=False)
 
 
 def test_capture_switch_leaves_output_bit_identical():
