@@ -104,6 +104,28 @@ vegas_status_t vegas_verify_attn_capture(
     int capture_row_a, int capture_row_b, float softmax_scale,
     void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * (1') Verify attention that allocates nothing.  The paper has no counterpart:
+ * this is a convenience for callers that cannot allocate device memory, for
+ * instance a plugin whose host framework owns every device allocation through
+ * its own pool, or a decode loop that must never call cudaMalloc because it
+ * can synchronise the device.  Same arguments and results as
+ * vegas_verify_attn_capture, without the workspace: the split-KV scratch lives
+ * in a fixed 16 MiB array inside the library's device memory (every GPU that
+ * loads the library holds it until exit).  Shapes whose
+ * vegas_verify_workspace_size() exceeds vegas_verify_noalloc_max_scratch_bytes()
+ * are rejected with VEGAS_ERR_WORKSPACE_TOO_SMALL.  The first call on a device
+ * looks up the array's device address, so make it before any stream capture.
+ * All calls share the array: each call clears its counters on `stream`, and
+ * calls whose GPU work overlaps (other streams or host threads) race.
+ */
+size_t vegas_verify_noalloc_max_scratch_bytes(void);
+
+vegas_status_t vegas_verify_attn_capture_noalloc(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
+    int score_stride, const int32_t* ctx_lens, int batch, int gamma,
+    int capture_row_a, int capture_row_b, float softmax_scale, void* stream);
+
 /* ------------------------------------------------------------------------
  * (2) Top-k select (§2.A argmax over |T| = k of the summed logits).
  *

@@ -85,6 +85,10 @@ _verify_ws = _sig("vegas_verify_workspace_size", _sz, [_P_KV, _i32, _i32])
 _verify = _sig("vegas_verify_attn_capture", _i32,
                [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32, _i32, _i32,
                 _f32, _c_void_p, _sz, _c_void_p])
+_verify_noalloc = _sig("vegas_verify_attn_capture_noalloc", _i32,
+                       [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32,
+                        _i32, _i32, _f32, _c_void_p])
+_noalloc_max = _sig("vegas_verify_noalloc_max_scratch_bytes", _sz, [])
 _select = _sig("vegas_select_topk", _i32,
                [_c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p])
 _sparse_ws = _sig("vegas_sparse_workspace_size", _sz, [_P_KV, _i32, _i32, _i32])
@@ -140,6 +144,21 @@ def vegas_verify_attn_capture(kv: PagedKV, q, out, scores, score_stride: int, ct
     _check(_verify(ctypes.byref(kv), _ptr(q), _ptr(out), _ptr(scores), score_stride,
                    _ptr(ctx_lens), batch, gamma, capture_row_a, capture_row_b, softmax_scale,
                    _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def vegas_verify_attn_capture_noalloc(kv: PagedKV, q, out, scores, score_stride: int, ctx_lens,
+                                      batch: int, gamma: int, capture_row_a: int,
+                                      capture_row_b: int, softmax_scale: float,
+                                      stream=None) -> None:
+    """vegas_verify_attn_capture without a workspace, for callers that cannot
+    allocate device memory; the scratch is a fixed array inside the library."""
+    _check(_verify_noalloc(ctypes.byref(kv), _ptr(q), _ptr(out), _ptr(scores), score_stride,
+                           _ptr(ctx_lens), batch, gamma, capture_row_a, capture_row_b,
+                           softmax_scale, _stream(stream)))
+
+
+def vegas_verify_noalloc_max_scratch_bytes() -> int:
+    return _noalloc_max()
 
 
 def vegas_select_topk(scores, score_stride: int, ctx_lens, k_per_seq, out_idx, batch: int,

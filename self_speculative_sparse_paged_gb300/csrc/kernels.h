@@ -65,6 +65,9 @@ struct SelectParams {
   int* err;
 };
 
+// Records `msg` as this host thread's vegas_last_error_detail(); returns status.
+int record_failure(int status, const char* msg);
+
 // Shared-memory bytes and launch of each kernel; return cudaError_t.
 
 // Largest 8-row query tile count per head_dim (d=128: 48 rows, d=64: 64 rows).

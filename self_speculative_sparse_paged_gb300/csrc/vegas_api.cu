@@ -220,6 +220,12 @@ cudaError_t launch_verify_any(const CUtensorMap& km, const CUtensorMap& vm,
 
 }  // namespace
 
+namespace vegas {
+int record_failure(int status, const char* msg) {
+  return (int)fail(static_cast<vegas_status_t>(status), "%s", msg);
+}
+}  // namespace vegas
+
 // =========================================================================
 // Verify attention with Collect-2-Query capture
 // =========================================================================

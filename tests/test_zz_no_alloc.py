@@ -1,0 +1,61 @@
+"""The verify entry point that allocates nothing, for callers that cannot call
+cudaMalloc (a plugin whose host framework owns all device memory, or a decode
+loop that must not risk cudaMalloc's device synchronisation).
+
+It must give the same results as vegas_verify_attn_capture with a caller
+workspace, on two calls in a row (the fixed scratch array is shared between
+calls and keeps the previous call's contents).  This file is collected last.
+"""
+import numpy as np
+import pytest
+import torch
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import self_speculative_sparse_paged_gb300 as vg  # noqa: E402
+from vegas_case import Case, assert_attention_close, bf16_to_f64  # noqa: E402
+from workload import configs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(c: Case):
+    w = c.w
+    out = torch.full_like(c.qv, float("nan"))
+    scores = torch.full((w.batch, w.hkv, c.stride), float("nan"), device="cuda")
+    vg.vegas_verify_attn_capture_noalloc(c.kv, c.qv, out, scores, c.stride, c.lens_t, w.batch,
+                                         w.gamma, 0, w.gamma, c.scale)
+    vg.vegas_read_device_status()
+    return out, scores
+
+
+@pytest.mark.parametrize("w", [
+    configs.QWEN3_8B_B1_32K.with_(ctx_lo=20000, ctx_hi=20000),
+    configs.QWEN3_8B_B8_48K_64K.with_(batch=3, ctx_lo=3000, ctx_hi=9000),
+], ids=["qwen_b1", "qwen_b3"])
+def test_noalloc_matches_workspace_entry_point_twice(w):
+    c = Case(w, device_gen=True)
+    assert 0 < vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma) <= \
+        vg.vegas_verify_noalloc_max_scratch_bytes()
+    ref_out, ref_scores = c.verify()
+    ref = bf16_to_f64(ref_out)
+    for _ in range(2):
+        out, scores = _noalloc(c)
+        assert_attention_close(bf16_to_f64(out), ref, "no-alloc verify output")
+        for b in range(w.batch):
+            L = int(c.lens[b])
+            got, exp = scores[b, :, :L].cpu().numpy(), ref_scores[b, :, :L].cpu().numpy()
+            np.testing.assert_allclose(got, exp, rtol=1e-5, atol=1e-4)
+
+
+def test_noalloc_rejects_shapes_beyond_the_scratch():
+    # 512 sequences x 8 KV heads: partials for 4096 units exceed the fixed array.
+    big = configs.QWEN3_8B_B8_48K_64K.with_(batch=512, ctx_lo=4000, ctx_hi=4000)
+    kv = vg.PagedKV(256, 256, 256, 256 * 512, 16, big.hq, big.hkv, big.head_dim, 256)
+    assert vg.vegas_verify_workspace_size(kv, big.batch, big.gamma) > \
+        vg.vegas_verify_noalloc_max_scratch_bytes()
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_capture_noalloc(kv, 256, 256, None, 1, 256, big.batch, big.gamma, 0,
+                                             big.gamma, 0.1, stream=0)
+    assert ei.value.status == 3
