@@ -164,9 +164,7 @@ class GpuIteration:
         self.scores = torch.empty((w.batch, w.hkv, self.stride), dtype=torch.float32, device=dev)
         self.idx = torch.empty((w.batch, w.hkv, self.k_max), dtype=torch.int32, device=dev)
         nv = vg.vegas_verify_workspace_size(self.kv[0], w.batch, w.gamma)
-        ns = vg.vegas_sparse_workspace_size(self.kv[0], w.batch, self.k_max, max(self.tails))
         self.ws_v = torch.zeros(max(nv, 256), dtype=torch.uint8, device=dev)
-        self.ws_s = torch.zeros(max(ns, 256), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(w.head_dim)
         self.launches_per_step = 2 + w.gamma
 
@@ -185,7 +183,7 @@ class GpuIteration:
         w = self.w
         self.vg.vegas_sparse_decode_attn(
             self.kv[r], self.qd[j], self.out_d[j], self.idx, self.k_max, self.kps_t, self.lens_t,
-            self.tl_t[j], self.tails[j], w.batch, self.scale, self.ws_s, self.ws_s.numel())
+            self.tl_t[j], self.tails[j], w.batch, self.scale)
 
     def step(self, r, ev=None, capture=True):
         if ev:

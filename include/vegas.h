@@ -153,16 +153,14 @@ vegas_status_t vegas_select_topk(
  * block table's range.
  *   q, out: device bf16 [batch][num_q_heads][head_dim]
  *   max_tail >= max_b tail_len[b]; k_per_seq[b] + tail_len[b] >= 1.
- * Supported: head_dim in {64, 128}, G <= 16.
+ * Needs no workspace (the split softmax states merge on chip).
+ * Supported: head_dim in {64, 128}, G <= 16, k_max + max_tail <= 16384.
  * ---------------------------------------------------------------------- */
-size_t vegas_sparse_workspace_size(const vegas_paged_kv_t* kv, int batch, int k_max,
-                                   int max_tail);
-
 vegas_status_t vegas_sparse_decode_attn(
     const vegas_paged_kv_t* kv, const void* q, void* out, const int32_t* idx,
     int k_max, const int32_t* k_per_seq, const int32_t* tail_start,
     const int32_t* tail_len, int max_tail, int batch, float softmax_scale,
-    void* workspace, size_t workspace_bytes, void* stream);
+    void* stream);
 
 /* ------------------------------------------------------------------------
  * Status.

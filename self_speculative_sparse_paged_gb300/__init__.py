@@ -20,7 +20,8 @@ from . import _build
 __all__ = [
     "VegasError", "PagedKV", "paged_kv", "lib", "library_path",
     "vegas_verify_workspace_size", "vegas_verify_attn_capture", "vegas_select_topk",
-    "vegas_sparse_workspace_size", "vegas_sparse_decode_attn", "vegas_synth_paged_kv",
+    "vegas_sparse_decode_attn", "vegas_synth_paged_kv", "vegas_verify_attn_capture_noalloc",
+    "vegas_verify_noalloc_max_scratch_bytes",
     "vegas_read_device_status", "vegas_status_string", "vegas_last_error_detail",
     "vegas_abi_version",
 ]
@@ -91,10 +92,9 @@ _verify_noalloc = _sig("vegas_verify_attn_capture_noalloc", _i32,
 _noalloc_max = _sig("vegas_verify_noalloc_max_scratch_bytes", _sz, [])
 _select = _sig("vegas_select_topk", _i32,
                [_c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p])
-_sparse_ws = _sig("vegas_sparse_workspace_size", _sz, [_P_KV, _i32, _i32, _i32])
 _sparse = _sig("vegas_sparse_decode_attn", _i32,
                [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p,
-                _i32, _i32, _f32, _c_void_p, _sz, _c_void_p])
+                _i32, _i32, _f32, _c_void_p])
 _synth = _sig("vegas_synth_paged_kv", _i32,
               [_c_void_p, _i32, _u64, _i32, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p,
                _c_void_p, _u64, _i32, _c_void_p, _c_void_p])
@@ -167,16 +167,12 @@ def vegas_select_topk(scores, score_stride: int, ctx_lens, k_per_seq, out_idx, b
                    batch, num_kv_heads, k_max, _stream(stream)))
 
 
-def vegas_sparse_workspace_size(kv: PagedKV, batch: int, k_max: int, max_tail: int) -> int:
-    return _sparse_ws(ctypes.byref(kv), batch, k_max, max_tail)
-
-
 def vegas_sparse_decode_attn(kv: PagedKV, q, out, idx, k_max: int, k_per_seq, tail_start,
                              tail_len, max_tail: int, batch: int, softmax_scale: float,
-                             workspace, workspace_bytes: int, stream=None) -> None:
+                             stream=None) -> None:
     _check(_sparse(ctypes.byref(kv), _ptr(q), _ptr(out), _ptr(idx), k_max, _ptr(k_per_seq),
                    _ptr(tail_start), _ptr(tail_len), max_tail, batch, softmax_scale,
-                   _ptr(workspace), workspace_bytes, _stream(stream)))
+                   _stream(stream)))
 
 
 def vegas_synth_paged_kv(cache, which: int, seed: int, layer: int, owner, num_pages: int,

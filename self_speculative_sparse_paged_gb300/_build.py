@@ -28,6 +28,7 @@ UNITS = [
     ("vegas_api.cu", "vegas_api.o", []),
     ("synth.cu", "synth.o", []),
     ("verify_noalloc.cu", "verify_noalloc.o", []),
+    ("verify_tc.cu", "verify_tc.o", []),
     ("select_topk.cu", "select_topk.o", []),
     ("sparse_decode.cu", "sparse_decode.o", []),
     ("verify_attn.cu", "verify_d128_c1.o", ["-DVEGAS_D=128", "-DVEGAS_CAP=1"]),

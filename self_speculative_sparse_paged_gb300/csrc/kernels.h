@@ -9,6 +9,8 @@ namespace vegas {
 
 constexpr int kAttnWarps = 8;          // warps per attention CTA
 constexpr int kMaxSplits = 128;        // split-KV partials per (sequence, KV head)
+constexpr int kMaxSparseCluster = 8;   // CTAs per (sequence, KV head) in the draft kernel
+constexpr int kMaxSparseRowsPerCta = 2048;
 
 struct VerifyParams {
   const void* q;            // bf16 [B][T][Hq][D]
@@ -45,11 +47,8 @@ struct SparseParams {
   int num_pages, max_pages;
   int hq, hkv, group;
   float scale_log2;
-  int rows_per_split;
-  int num_splits;
-  int* tickets;
-  float* part_ml;
-  float* part_o;
+  int rows_per_split;       // list entries per CTA of the cluster
+  int num_splits;           // CTAs per cluster (one cluster per unit)
   int* err;
 };
 
@@ -72,12 +71,18 @@ int record_failure(int status, const char* msg);
 
 // Largest 8-row query tile count per head_dim (d=128: 48 rows, d=64: 64 rows).
 inline int verify_max_ntiles(int head_dim) { return head_dim == 128 ? 6 : 8; }
+// tcgen05 verify kernel (head_dim 128, at most 32 query columns incl. capture);
+// its splits must cover whole 8-page tiles.
+constexpr int kTcMaxColumns = 32;
+constexpr int kTcPagesPerTile = 8;
+cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const VerifyParams& p, int ncols, bool capture, int batch,
+                             cudaStream_t stream);
 template <int D, bool CAP>
 cudaError_t launch_verify_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
                             const VerifyParams& p, int ntiles, int batch, cudaStream_t stream);
 
 size_t sparse_smem_bytes(int head_dim, int ntiles);
-int sparse_max_rows_per_split();
 cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int batch,
                           cudaStream_t stream);
 

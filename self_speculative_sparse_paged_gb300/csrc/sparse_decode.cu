@@ -8,39 +8,49 @@
 //
 // Here the selected positions stay logical token positions: each is mapped
 // through the block table of the 16-token paged cache, so the same cache
-// serves verify and draft.  Grid (num_splits, Hkv, B); a CTA owns a
-// contiguous range of the unit's list "T then tail".  It first resolves every
-// entry of its range to a cache row (position -> page -> row) in shared
-// memory, then each warp gathers 16-entry groups with one 1-D bulk copy per
-// K row and per V row (lanes 0-15 K, 16-31 V) into padded rows, and runs the
-// same warp core as the verify kernel with the G query heads of the group as
-// the tile's columns.
+// serves verify and draft.  One thread-block cluster of CL CTAs per
+// (KV head, sequence); CTA r owns a contiguous range of the unit's list
+// "T then tail".  It first resolves every entry of its range to a cache row
+// (position -> page -> row) in shared memory, then each warp gathers 16-entry
+// groups with one 1-D bulk copy per K row and per V row (lanes 0-15 K, 16-31
+// V) into padded rows and runs the same warp core as the verify kernel with
+// the G query heads of the group as the tile's columns.  The CTAs' softmax
+// states meet in distributed shared memory: rank 0 merges them and writes the
+// output, with no global scratch and no second pass.
+#include <cooperative_groups.h>
+
 #include "kernels.h"
 #include "split_merge.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace vegas {
 
 template <int D>
 struct SparseCfg {
-  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kStages = 2;
   static constexpr int kRow = D * 2 + 16;           // padded row stride
   static constexpr int kTile = 16 * kRow;
   static constexpr int kStage = 2 * kTile;
-  static constexpr int kMaxRowsPerSplit = 1024;
+  static constexpr int kMaxRows = kMaxSparseRowsPerCta;
+  static constexpr size_t kStageBytes = size_t(kAttnWarps) * kStages * kStage;
 };
 
 template <int D, int NT>
 constexpr size_t sparse_smem_layout_bytes() {
-  return size_t(kAttnWarps) * SparseCfg<D>::kStages * SparseCfg<D>::kStage   // stages
-         + size_t(NT) * 8 * (2 * D + 16)                                     // Q tile
-         + size_t(kAttnWarps) * SparseCfg<D>::kStages * 8                    // mbarriers
-         + size_t(SparseCfg<D>::kMaxRowsPerSplit) * 4                        // row table
+  return SparseCfg<D>::kStageBytes                                 // stages
+         + size_t(NT) * 8 * (2 * D + 16)                           // Q tile
+         + size_t(kAttnWarps) * SparseCfg<D>::kStages * 8          // mbarriers
+         + size_t(SparseCfg<D>::kMaxRows) * 4                      // row table
+         + size_t(NT) * 8 * (D + 2) * 4                            // CTA partial
+         + size_t(kMaxSparseCluster) * NT * 8 * 4                  // rank-0 weights
          + 1024;
 }
 
 template <int D, int NT>
 __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const SparseParams p) {
   constexpr int W = kAttnWarps;
+  constexpr int NTH = W * 32;
   constexpr int NPAD = NT * 8;
   constexpr int STAGES = SparseCfg<D>::kStages;
   constexpr int ROW = SparseCfg<D>::kRow;
@@ -49,43 +59,52 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   constexpr int QROW = 2 * D + 16;
   using Tile = PaddedTile<D>;
 
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int CL = (int)cluster.num_blocks();
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* stage_area = smem;
-  uint8_t* qs = smem + W * STAGES * STAGE;
+  uint8_t* qs = smem + SparseCfg<D>::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(qs + NPAD * QROW);
   int32_t* rows = reinterpret_cast<int32_t*>(bars + W * STAGES);
+  float* pM = reinterpret_cast<float*>(rows + SparseCfg<D>::kMaxRows);   // [NPAD] CTA partial
+  float* pL = pM + NPAD;                                                 // [NPAD]
+  float* pO = pL + NPAD;                                                 // [NPAD][D]
+  float* wts = pO + NPAD * D;                                            // [8][NPAD] rank-0 weights
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int g = blockIdx.y, b = blockIdx.z;
   const int unit = b * p.hkv + g;
   const int cap = p.max_pages * 16;
 
   int kb = p.k_per_seq[b];
   if (kb < 0 || kb > p.k_max) {
-    if (tid == 0 && g == 0 && split == 0) set_error(p.err, kErrDeviceFault);
+    if (tid == 0 && g == 0 && rank == 0) set_error(p.err, kErrDeviceFault);
     kb = max(0, min(kb, p.k_max));
   }
   const int tstart = p.tail_start[b];
   const int tlen = max(0, p.tail_len[b]);
   const int total = kb + tlen;
-  const int rbeg = split * p.rows_per_split;
+  const int rbeg = rank * p.rows_per_split;
   const int rend = min(rbeg + p.rows_per_split, total);
   const int nrows = max(0, rend - rbeg);
 
   if (tid == 0) {
-    for (int i = 0; i < W * STAGES; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    // one arrival per lane per stage use: each lane's cp.async copies signal it
+    for (int i = 0; i < W * STAGES; ++i) mbar_init(smem_u32(&bars[i]), 32);
     fence_mbar_init();
   }
   // Entry e of the list: T[e] for e < k_b, else tail_start + (e - k_b).
   // Resolved in batches: every index load of a thread, then every page load.
-  constexpr int kPer = SparseCfg<D>::kMaxRowsPerSplit / (W * 32);
+  constexpr int kPer = SparseCfg<D>::kMaxRows / NTH;
   {
     int pos[kPer], phys[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      const int i = tid + u * W * 32;
+      const int i = tid + u * NTH;
       const int e = rbeg + i;
       pos[u] = 0;
       if (i < nrows) pos[u] = e < kb ? __ldcg(&p.idx[size_t(unit) * p.k_max + e]) : tstart + (e - kb);
@@ -96,11 +115,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
         set_error(p.err, kErrDeviceFault);
         pos[u] = 0;
       }
-      phys[u] = tid + u * W * 32 < nrows ? __ldg(&p.block_table[size_t(b) * p.max_pages + (pos[u] >> 4)]) : 0;
+      phys[u] = tid + u * NTH < nrows ? __ldg(&p.block_table[size_t(b) * p.max_pages + (pos[u] >> 4)]) : 0;
     }
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      const int i = tid + u * W * 32;
+      const int i = tid + u * NTH;
       if (i < nrows) {
         if (phys[u] < 0 || phys[u] >= p.num_pages) {
           set_error(p.err, kErrDeviceFault);
@@ -110,7 +129,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
       }
     }
   }
-  for (int i = tid; i < NPAD * (D / 8); i += W * 32) {
+  for (int i = tid; i < NPAD * (D / 8); i += NTH) {
     const int n = i / (D / 8), c = i % (D / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
     if (n < p.group) {
@@ -129,20 +148,25 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(p.k_cache);
   const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(p.v_cache);
 
-  // Every lane issues one row copy; rows past the range repeat the group's
-  // first row (masked later) so the byte count per stage is constant.
+  // The warp copies the group's 16 K rows and 16 V rows with 16-byte cp.async
+  // (consecutive lanes cover consecutive 16-byte chunks of a row); rows past
+  // the range repeat the group's first row (masked later).  Each lane then
+  // arrives on the stage barrier when its own copies have landed.
+  constexpr int CPR = D / 8;                       // 16-byte chunks per row
   auto issue = [&](int i) {
     const int grp = warp + i * W;
     const int s = i % STAGES;
-    const uint32_t bar = bar0 + s * 8;
-    if (lane == 0) mbar_arrive_expect_tx(bar, 32 * D * 2);   // 32 rows of D bf16
-    __syncwarp();
-    const int r = lane & 15;
-    const int li = grp * 16 + r;
-    const int row = rows[li < nrows ? li : grp * 16];
-    const __nv_bfloat16* src = (lane < 16 ? kc : vc) + size_t(row) * D;
-    const uint32_t dst = stage0 + s * STAGE + (lane < 16 ? 0 : TILE) + r * ROW;
-    bulk_load(dst, src, D * 2, bar);
+#pragma unroll
+    for (int j = 0; j < (32 * CPR) / 32; ++j) {
+      const int c = lane + 32 * j;                 // chunk of the 32 rows (K rows, then V rows)
+      const int r32 = c / CPR, cc = c % CPR;
+      const int r = r32 & 15;
+      const int li = grp * 16 + r;
+      const int row = rows[li < nrows ? li : grp * 16];
+      const __nv_bfloat16* src = (r32 < 16 ? kc : vc) + size_t(row) * D + cc * 8;
+      cp_async16(stage0 + s * STAGE + (r32 < 16 ? 0 : TILE) + r * ROW + cc * 16, src);
+    }
+    cp_async_arrive_noinc(bar0 + s * 8);
   };
   for (int i = 0; i < min(STAGES, nmy); ++i) issue(i);
 
@@ -189,24 +213,39 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   }
   reduce_row_sums<D, NT>(st);
   __syncthreads();
+  cta_merge_to_smem<D, NT, W>(st, stage_area, SparseCfg<D>::kStageBytes, p.group, pM, pL, pO);
 
-  SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-  auto out_row = [&](int n) { return out + (size_t(b) * p.hq + g * p.group + n) * D; };
-  merge_and_write<D, NT, W>(st, stage_area, size_t(W) * STAGES * STAGE, p.group, unit, split,
-                            p.num_splits, ws, out_row);
+  // Cluster merge: rank 0 weighs every CTA's state through distributed shared
+  // memory, M = max_r m_r, w_r = 2^(m_r - M) / sum_r 2^(m_r - M) l_r.
+  cluster.sync();
+  if (rank == 0) {
+    for (int n = tid; n < p.group; n += NTH) {
+      float M = -INFINITY;
+      for (int r = 0; r < CL; ++r) M = fmaxf(M, cluster.map_shared_rank(pM, r)[n]);
+      float L = 0.f;
+      for (int r = 0; r < CL; ++r) {
+        const float f = ex2(cluster.map_shared_rank(pM, r)[n] - M);
+        wts[r * NPAD + n] = f;
+        L += f * cluster.map_shared_rank(pL, r)[n];
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int r = 0; r < CL; ++r) wts[r * NPAD + n] *= inv;
+    }
+    __syncthreads();
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    for (int e = tid; e < p.group * D; e += NTH) {
+      const int n = e / D;
+      float a = 0.f;
+      for (int r = 0; r < CL; ++r) a += wts[r * NPAD + n] * cluster.map_shared_rank(pO, r)[e];
+      out[(size_t(b) * p.hq + g * p.group + n) * D + (e % D)] = __float2bfloat16_rn(a);
+    }
+  }
+  cluster.sync();   // no CTA leaves while rank 0 may still read its shared memory
 }
-
-size_t sparse_smem_bytes(int head_dim, int ntiles) {
-  (void)ntiles;
-  return head_dim == 128 ? sparse_smem_layout_bytes<128, 2>() : sparse_smem_layout_bytes<64, 2>();
-}
-
-int sparse_max_rows_per_split() { return SparseCfg<128>::kMaxRowsPerSplit; }
 
 template <int D, int NT>
 static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStream_t stream) {
-  const size_t smem = sparse_smem_bytes(D, NT);
+  constexpr size_t smem = sparse_smem_layout_bytes<D, NT>();
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<D, NT>,
@@ -214,13 +253,24 @@ static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStrea
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(p.num_splits, p.hkv, batch);
-  sparse_decode_kernel<D, NT><<<grid, kAttnWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits, p.hkv, batch);
+  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.num_splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<D, NT>, p);
 }
 
 cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int batch,
                           cudaStream_t stream) {
+  if (p.num_splits < 1 || p.num_splits > kMaxSparseCluster) return cudaErrorInvalidValue;
   if (head_dim == 128) {
     if (ntiles == 1) return launch_sparse_one<128, 1>(p, batch, stream);
     if (ntiles == 2) return launch_sparse_one<128, 2>(p, batch, stream);

@@ -156,7 +156,8 @@ int verify_splits(int units, int max_pages, int sms) {
 }
 
 struct VerifyPlan {
-  int nq, ntiles, splits, pages_per_split;
+  int nq, ncols, ntiles, splits, pages_per_split;
+  bool tc;   // tcgen05 kernel (head_dim 128, <= 32 columns) instead of the mma.sync one
   size_t tickets_off, ml_off, o_off, bytes;
 };
 
@@ -169,11 +170,15 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
   VerifyPlan pl{};
   const int G = kv->num_q_heads / kv->num_kv_heads;
   pl.nq = (gamma + 1) * G;
-  pl.ntiles = (verify_columns(pl.nq, capture) + 7) / 8;
+  pl.ncols = verify_columns(pl.nq, capture);
+  pl.ntiles = (pl.ncols + 7) / 8;
+  pl.tc = kv->head_dim == 128 && pl.ncols <= vegas::kTcMaxColumns;
   const int units = std::max(1, batch * kv->num_kv_heads);
   pl.splits = verify_splits(units, kv->max_pages_per_seq, sms);
   pl.pages_per_split = (kv->max_pages_per_seq + pl.splits - 1) / pl.splits;
-  pl.pages_per_split += pl.pages_per_split & 1;   // kernels step over page pairs
+  // splits cover whole tiles: 8 pages (tcgen05 kernel) or page pairs
+  const int quantum = pl.tc ? vegas::kTcPagesPerTile : 2;
+  pl.pages_per_split = (pl.pages_per_split + quantum - 1) / quantum * quantum;
   pl.splits = (kv->max_pages_per_seq + pl.pages_per_split - 1) / pl.pages_per_split;
   pl.tickets_off = 0;
   pl.ml_off = align256(size_t(units) * 4);
@@ -183,28 +188,24 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
 }
 
 struct SparsePlan {
-  int ntiles, splits, rows_per_split;
-  size_t tickets_off, ml_off, o_off, bytes;
+  int ntiles, cluster, rows_per_cta;
 };
 
+// One cluster of up to 8 CTAs per (sequence, KV head), each CTA at least 64
+// entries of the list (fewer CTAs when the list is short or the units many).
 SparsePlan plan_sparse(const vegas_paged_kv_t* kv, int batch, int k_max, int max_tail, int sms) {
   SparsePlan pl{};
   const int G = kv->num_q_heads / kv->num_kv_heads;
   pl.ntiles = (G + 7) / 8;
   const int units = std::max(1, batch * kv->num_kv_heads);
   const int rows_max = std::max(1, k_max + max_tail);
-  const int cap = vegas::sparse_max_rows_per_split();
-  int s = std::max((sms + units - 1) / units, (rows_max + cap - 1) / cap);
-  s = std::min(s, std::max(1, (rows_max + 15) / 16));
-  s = std::min(s, vegas::kMaxSplits);
-  int rps = (rows_max + s - 1) / s;
-  rps = (rps + 15) / 16 * 16;
-  pl.rows_per_split = rps;
-  pl.splits = (rows_max + rps - 1) / rps;
-  pl.tickets_off = 0;
-  pl.ml_off = align256(size_t(units) * 4);
-  pl.o_off = pl.ml_off + align256(size_t(units) * pl.splits * G * 2 * 4);
-  pl.bytes = pl.o_off + size_t(units) * pl.splits * G * kv->head_dim * 4;
+  int cl = std::min(vegas::kMaxSparseCluster, std::max(1, (rows_max + 63) / 64));
+  while (cl > 1 && (long long)units * (cl / 2) >= 2LL * sms &&
+         (rows_max + cl / 2 - 1) / (cl / 2) <= vegas::kMaxSparseRowsPerCta)
+    cl /= 2;
+  int rpc = (rows_max + cl - 1) / cl;
+  pl.rows_per_cta = (rpc + 15) / 16 * 16;
+  pl.cluster = cl;
   return pl;
 }
 
@@ -231,7 +232,9 @@ int record_failure(int status, const char* msg) {
 // =========================================================================
 VEGAS_API size_t vegas_verify_workspace_size(const vegas_paged_kv_t* kv, int batch, int gamma) {
   if (check_kv(kv) != VEGAS_OK || batch < 0 || gamma < 0) return 0;
-  return plan_verify(kv, batch, gamma, current_sms()).bytes;
+  const int sms = current_sms();
+  return std::max(plan_verify(kv, batch, gamma, sms, true).bytes,
+                  plan_verify(kv, batch, gamma, sms, false).bytes);
 }
 
 VEGAS_API vegas_status_t vegas_verify_attn_capture(
@@ -298,8 +301,11 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   p.part_ml = ws ? reinterpret_cast<float*>(ws + pl.ml_off) : nullptr;
   p.part_o = ws ? reinterpret_cast<float*>(ws + pl.o_off) : nullptr;
   p.err = err;
-  cudaError_t e = launch_verify_any(km, vm, p, kv->head_dim, pl.ntiles, scores != nullptr, batch,
-                                    static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      pl.tc ? vegas::launch_verify_tc(km, vm, p, pl.ncols, scores != nullptr, batch,
+                                      static_cast<cudaStream_t>(stream))
+            : launch_verify_any(km, vm, p, kv->head_dim, pl.ntiles, scores != nullptr, batch,
+                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return VEGAS_OK;
 }
@@ -346,16 +352,10 @@ VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride
 // =========================================================================
 // Sparse draft-decode attention
 // =========================================================================
-VEGAS_API size_t vegas_sparse_workspace_size(const vegas_paged_kv_t* kv, int batch, int k_max,
-                                             int max_tail) {
-  if (check_kv(kv) != VEGAS_OK || batch < 0 || k_max < 0 || max_tail < 0) return 0;
-  return plan_sparse(kv, batch, k_max, max_tail, current_sms()).bytes;
-}
-
 VEGAS_API vegas_status_t vegas_sparse_decode_attn(
     const vegas_paged_kv_t* kv, const void* q, void* out, const int32_t* idx, int k_max,
     const int32_t* k_per_seq, const int32_t* tail_start, const int32_t* tail_len, int max_tail,
-    int batch, float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+    int batch, float softmax_scale, void* stream) {
   vegas_status_t st = check_kv(kv);
   if (st != VEGAS_OK) return st;
   if (batch < 0 || k_max < 0 || max_tail < 0)
@@ -371,14 +371,10 @@ VEGAS_API vegas_status_t vegas_sparse_decode_attn(
   int* err = nullptr;
   int sms = 0;
   if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
+  if (k_max + max_tail > vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta)
+    return fail(VEGAS_ERR_UNSUPPORTED, "k_max + max_tail = %d exceeds %d", k_max + max_tail,
+                vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta);
   const SparsePlan pl = plan_sparse(kv, batch, k_max, max_tail, sms);
-  if (pl.splits > 1) {
-    if (!workspace || workspace_bytes < pl.bytes)
-      return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "sparse workspace %zu < %zu bytes",
-                  workspace_bytes, pl.bytes);
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-      return fail(VEGAS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  }
   vegas::SparseParams p{};
   p.q = q;
   p.out = out;
@@ -396,12 +392,8 @@ VEGAS_API vegas_status_t vegas_sparse_decode_attn(
   p.hkv = kv->num_kv_heads;
   p.group = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.rows_per_split = pl.rows_per_split;
-  p.num_splits = pl.splits;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.tickets = ws ? reinterpret_cast<int*>(ws + pl.tickets_off) : nullptr;
-  p.part_ml = ws ? reinterpret_cast<float*>(ws + pl.ml_off) : nullptr;
-  p.part_o = ws ? reinterpret_cast<float*>(ws + pl.o_off) : nullptr;
+  p.rows_per_split = pl.rows_per_cta;
+  p.num_splits = pl.cluster;
   p.err = err;
   cudaError_t e = vegas::launch_sparse(p, kv->head_dim, pl.ntiles, batch,
                                        static_cast<cudaStream_t>(stream));

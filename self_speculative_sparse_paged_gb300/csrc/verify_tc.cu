@@ -1,0 +1,534 @@
+// Verify attention with Collect-2-Query capture on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory), head_dim 128.
+//
+// Same contract as the mma.sync kernel in verify_attn.cu ("Vegas:
+// Self-Speculative Decoding with Verification-Guided Sparse Attention",
+// gist.science technical summary, §2 "Core mechanism", §2.A, §2.B
+// "Collect-2-Query", §3 "Implementation"), used when the unit's query columns
+// (the (gamma+1)*G rows plus the two capture columns) fit in 32.
+//
+// One CTA per (split, KV head, sequence), 10 warps:
+//   warp 0     TMA producer: lanes 0..7 each load one page of K and of V of a
+//              128-position tile (8 pages) into a 3-deep ring of stages;
+//   warp 1     allocates tensor memory; lane 0 issues the MMAs
+//                S^T[128 pos x N] = K[128 x 128] . Q^T   (both K-major, the K
+//                tile consumed straight from the TMA's 128-byte swizzle),
+//                O^T[128 d x N]  += V^T[128 x 128] . P^T (V read MN-major);
+//   warps 2-5  softmax group 0 (even tiles), warps 6-9 group 1 (odd tiles):
+//              thread i of a group owns tensor-memory lane i, i.e. tile
+//              position i for S and head dimension i for its O^T accumulator.
+// Each group keeps its own running maxima, row sums and O^T accumulator in
+// tensor memory (the two are merged at the end, like two splits).  Per tile a
+// softmax thread loads its position's logits, writes the captured score (the
+// two capture columns hold the summed captured query, so the score is their
+// sum), masks, and raises the running maxima only when a logit exceeds them by
+// 8 (one vote per group); only then is the group's O^T rescaled in tensor
+// memory.  It writes P^T = 2^(x - m) as bf16 into a 128-byte-swizzled shared
+// buffer that the PV MMA reads.
+#include "kernels.h"
+#include "split_merge.cuh"
+
+namespace vegas {
+
+template <int NQP, int NQC>
+struct TcCfg {
+  static constexpr int D = 128;
+  // K and V tiles live in separate rings: a K slot frees when its S MMA
+  // completes, a V slot only when its PV MMA does, so V gets the deeper ring.
+  static constexpr int KS = 2;
+  static constexpr int VS = 4;
+  static constexpr int kKV = 128 * D * 2;            // one K (or V) tile, 32 KB
+  static constexpr int kQ = 2 * NQP * 128;           // Q^T operand [half][NQP][128 B]
+  static constexpr int kP = 2 * NQP * 128;           // P^T operand [kblock][NQP][128 B]
+  static constexpr int kThreads = 352;               // 11 warps
+  static constexpr uint32_t kTmemCols = 128;         // S0, S1, O0, O1 at columns 0, 32, 64, 96
+  static constexpr int kOffV = KS * kKV;
+  static constexpr int kOffQ = (KS + VS) * kKV;
+  static constexpr int kOffP = kOffQ + kQ;
+  static constexpr int kOffBar = kOffP + 2 * kP;
+  static constexpr int kNumBars = 2 * KS + 2 * VS + 4 * 2 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  // misc: tmem slot, flag, votes[2][4], colmax[2][4][NQC], colsum[2][4][NQC],
+  // gm[2][NQC], gl[2][NQC], tlim[NQP]
+  static constexpr size_t kMisc = 16 + 32 + 4 * (16 * NQC + 4 * NQC + NQP);
+  static constexpr size_t kSmem = size_t(kOffMisc) + kMisc + 1024;
+};
+
+template <int NQP, int NQC, bool CAPTURE>
+__global__ void __launch_bounds__(352, 1)
+    verify_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const VerifyParams p) {
+  using Cfg = TcCfg<NQP, NQC>;
+  constexpr int D = 128;
+  constexpr int KS = Cfg::KS;
+  constexpr int VS = Cfg::VS;
+  static_assert(NQP == 16 || NQP == 32, "MMA N");
+  static_assert(NQC % 8 == 0 && NQC <= NQP, "processed columns");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint8_t* qs = smem + Cfg::kOffQ;
+  const uint32_t bar0 = sbase + Cfg::kOffBar;
+  // barriers: K full/free (per K slot), V full/free (per V slot); S full, S
+  // read, P ready, PV done (per softmax group); MMA drain
+  auto kfull = [&](int s) { return bar0 + 8 * s; };
+  auto kfree = [&](int s) { return bar0 + 8 * (KS + s); };
+  auto vfull = [&](int s) { return bar0 + 8 * (2 * KS + s); };
+  auto vfree = [&](int s) { return bar0 + 8 * (2 * KS + VS + s); };
+  constexpr int B1 = 2 * KS + 2 * VS;
+  auto sfull = [&](int g2) { return bar0 + 8 * (B1 + g2); };
+  auto sread = [&](int g2) { return bar0 + 8 * (B1 + 2 + g2); };
+  auto pready = [&](int g2) { return bar0 + 8 * (B1 + 4 + g2); };
+  auto pvdone = [&](int g2) { return bar0 + 8 * (B1 + 6 + g2); };
+  const uint32_t drain = bar0 + 8 * (B1 + 8);
+  uint8_t* misc = smem + Cfg::kOffMisc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  int* flag = reinterpret_cast<int*>(misc + 4);
+  int* votes = reinterpret_cast<int*>(misc + 16);                // [2][4]
+  float* colmax = reinterpret_cast<float*>(misc + 48);           // [2][4][NQC]
+  float* colsum = colmax + 8 * NQC;                              // [2][4][NQC]
+  float* gm = colsum + 8 * NQC;                                  // [2][NQC]
+  float* gl = gm + 2 * NQC;                                      // [2][NQC]
+  int* tlim = reinterpret_cast<int*>(gl + 2 * NQC);              // [NQP]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int unit = b * p.hkv + g;
+  const int T = p.gamma + 1;
+  const int cap = p.max_pages * 16;
+  int L = p.ctx_lens[b];
+  if (L < 0 || L + T > cap) {
+    if (tid == 0) set_error(p.err, kErrDeviceFault);
+    L = max(0, min(L, cap - T));
+  }
+  const int npages = (L + T + 15) / 16;
+  const int pbeg = split * p.pages_per_split;
+  const int pend = min(pbeg + p.pages_per_split, npages);
+  const int ntiles = pend > pbeg ? (pend - pbeg + 7) / 8 : 0;
+  const int cap0 = (p.nq + 1) & ~1;
+  const int last_valid = L + p.gamma;
+
+  if (tid == 0) {
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(kfull(s), 1);
+      mbar_init(kfree(s), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(vfull(s), 1);
+      mbar_init(vfree(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sfull(i), 1);
+      mbar_init(sread(i), 128);
+      mbar_init(pready(i), 128);
+      mbar_init(pvdone(i), 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();   // barriers initialised before anyone waits on them
+  // Warps 0 and 10 start streaming K and V right away; warps 1-9 meanwhile
+  // allocate tensor memory and build the Q^T operand.
+  constexpr int SN = 288;                      // threads of warps 1..9
+  uint32_t tmem = 0;
+  if (warp >= 1 && warp <= 9) {
+    const int st = tid - 32;
+    if (warp == 1) {
+      tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+      tmem_relinquish();
+    }
+    // Q^T operand, K-major with the 128-byte swizzle: element (n, k) at
+    // (k / 64) * NQP * 128 + n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16 + (k % 8) * 2.
+    for (int i = st; i < NQP * 16; i += SN) {
+      const int n = i >> 4, c = i & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n < p.nq) {
+        const int t = n / p.group, hl = n - t * p.group;
+        v = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                           ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D)[c];
+      }
+      *reinterpret_cast<uint4*>(qs + (c >> 3) * (NQP * 128) + n * 128 + (((c & 7) ^ (n & 7)) << 4)) = v;
+    }
+    for (int n = st; n < NQP; n += SN) tlim[n] = n < p.nq ? min(n / p.group, p.gamma) : -1;
+    if (CAPTURE) {
+      named_bar(4, SN);
+      // the summed captured query as a bf16 part and a bf16 remainder, summed
+      // from the Q tile just written (rows t * G .. t * G + G - 1 of each row t)
+      auto qoff = [&](int n, int k) {
+        return (k >> 6) * (NQP * 128) + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
+      };
+      for (int j = st; j < D; j += SN) {
+        float acc = 0.f;
+        for (int r = 0; r < 2; ++r) {
+          if (r == 1 && p.row_b == p.row_a) break;
+          const int t = r == 0 ? p.row_a : p.row_b;
+          for (int hl = 0; hl < p.group; ++hl)
+            acc += __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16*>(qs + qoff(t * p.group + hl, j)));
+        }
+        const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat16*>(qs + qoff(cap0, j)) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(qs + qoff(cap0 + 1, j)) = lo;
+      }
+    }
+    // Generic-proxy writes of Q must be visible to the tensor cores (async proxy).
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar(4, SN);
+    tc_fence_after();
+    tmem = *tmem_slot;
+  }
+  bool ok = true;
+
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // warp 0 streams the K tiles, warp 10 the V tiles, each through its ring;
+    // lanes 0..7 load one page (two 64-column boxes) of the tile each.
+    const bool is_k = warp == 0;
+    const int depth = is_k ? KS : VS;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    const uint32_t ring = sbase + (is_k ? 0 : Cfg::kOffV);
+    const int32_t* bt_row = p.block_table + size_t(b) * p.max_pages;
+    int issued = 0;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int s = t % depth;
+      const uint32_t full = is_k ? kfull(s) : vfull(s);
+      const uint32_t freed = is_k ? kfree(s) : vfree(s);
+      if (t >= depth && !mbar_wait_bounded(freed, ((t / depth) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      int page = pbeg + 8 * t + (lane & 7);
+      if (page >= pend) page = pbeg + 8 * t;          // loaded again, masked by the softmax
+      int phys = lane < 8 ? __ldg(&bt_row[page]) : 0;
+      if (lane < 8 && (phys < 0 || phys >= p.num_pages)) {
+        set_error(p.err, kErrDeviceFault);
+        phys = 0;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(full, Cfg::kKV);
+      __syncwarp();
+      if (lane < 8) {
+        const int row = (phys * p.hkv + g) * 16;
+        const uint32_t dst = ring + s * Cfg::kKV + lane * 2048;
+        tma_load_2d(dst, map, 0, row, full);
+        tma_load_2d(dst + 16384, map, 64, row, full);
+      }
+      __syncwarp();
+      issued = t + 1;
+    }
+    if (!ok) {
+      if (lane == 0) set_error(p.err, kErrDeviceTimeout);
+      for (int t = max(0, issued - depth); t < issued; ++t)
+        (void)mbar_wait_bounded(is_k ? kfull(t % depth) : vfull(t % depth), (t / depth) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, NQP, 0, 0);
+      constexpr uint32_t idPV = idesc_bf16(128, NQP, 1, 0);
+      auto issue_pv = [&](int t) -> bool {
+        const int gg = t & 1, s = t % VS;
+        if (!mbar_wait_bounded(pready(gg), (t >> 1) & 1)) return false;
+        if (!mbar_wait_bounded(vfull(s), (t / VS) & 1)) return false;
+        tc_fence_after();
+        const uint32_t vb = sbase + Cfg::kOffV + s * Cfg::kKV;
+        const uint32_t pb = sbase + Cfg::kOffP + gg * Cfg::kP;
+#pragma unroll
+        for (int kp = 0; kp < 8; ++kp) {
+          const uint64_t a = smem_desc(vb + kp * 2048, 16384, 1024, 2);
+          const uint64_t bd = smem_desc(pb + (kp >> 2) * (NQP * 128) + (kp & 3) * 32, 16, 1024, 2);
+          tc_mma(tmem + 64 + 32 * gg, a, bd, idPV, t >= 2 || kp > 0);
+        }
+        tc_commit(pvdone(gg));
+        tc_commit(vfree(s));
+        return true;
+      };
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const int s = t % KS, gg = t & 1;
+        if (!mbar_wait_bounded(kfull(s), (t / KS) & 1)) { ok = false; break; }
+        if (t >= 2 && !mbar_wait_bounded(sread(gg), ((t >> 1) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = sbase + s * Cfg::kKV;
+        const uint32_t qb = sbase + Cfg::kOffQ;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t a = smem_desc(kb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2);
+          const uint64_t bd = smem_desc(qb + (ks >> 2) * (NQP * 128) + (ks & 3) * 32, 16, 1024, 2);
+          tc_mma(tmem + 32 * gg, a, bd, idS, ks > 0);
+        }
+        tc_commit(sfull(gg));
+        tc_commit(kfree(s));
+        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+      }
+      if (ok && ntiles > 0 && !issue_pv(ntiles - 1)) ok = false;
+      if (!ok) set_error(p.err, kErrDeviceTimeout);
+      // every MMA issued has completed before tensor memory is released
+      tc_commit(drain);
+      (void)mbar_wait_bounded(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax groups (warps 2-9)
+    const int grp = (warp - 2) >> 2;          // 0: even tiles, 1: odd tiles
+    const int q4 = warp & 3;                  // tensor-memory lane quarter of this warp
+    const int i = 32 * q4 + lane;             // tile position / head dimension owned
+    const uint32_t tl = tmem + (uint32_t(32 * q4) << 16);
+    const uint32_t s_col = 32 * grp, o_col = 64 + 32 * grp;
+    float m[NQC], ls[NQC];
+#pragma unroll
+    for (int n = 0; n < NQC; ++n) {
+      m[n] = kEmptyMax;
+      ls[n] = 0.f;
+    }
+    uint32_t colbits = 0;
+#pragma unroll
+    for (int n = 0; n < NQC; ++n)
+      if (n < p.nq) colbits |= 1u << n;
+    float* srow = CAPTURE ? p.scores + size_t(unit) * p.score_stride : nullptr;
+    int Lcap = L;
+    if (CAPTURE && L > p.score_stride) {
+      if (i == 0 && grp == 0) set_error(p.err, kErrDeviceFault);
+      Lcap = p.score_stride;
+    }
+    int mytiles = 0;
+    // A failed (timed-out) wait is carried to the group vote below, so the 128
+    // threads of a group always leave the loop together.
+    for (int t = grp; t < ntiles; t += 2) {
+      const int k = t >> 1, s = t % VS;
+      bool okt = ok && mbar_wait_bounded(sfull(grp), k & 1);
+      tc_fence_after();
+      float x[NQC];
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) x[n] = 0.f;
+      if (okt) {
+#pragma unroll
+        for (int c = 0; c < NQC / 8; ++c) {
+          float v8[8];
+          tmem_ld8(tl + s_col + 8 * c, v8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[8 * c + e] = v8[e];
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(sread(grp));
+      }
+      const int page = pbeg + 8 * t + (i >> 4);
+      const bool live = page < pend;
+      const int pos = page * 16 + (i & 15);
+      if (CAPTURE && okt && live && pos < Lcap) {
+        float c = 0.f;
+#pragma unroll
+        for (int n = 0; n < NQC; ++n)
+          if (n == cap0 || n == cap0 + 1) c += x[n];
+        srow[pos] = c * p.scale;
+      }
+      const int lpos = (live ? page : pbeg + 8 * t) * 16 + (i & 15);   // position loaded in row i
+      if (okt && lpos > last_valid) {
+        // a cache slot past the window: zero its V row so 0 * garbage cannot be NaN
+        okt = mbar_wait_bounded(vfull(s), (t / VS) & 1);
+        uint8_t* vrow = smem + Cfg::kOffV + s * Cfg::kKV + i * 128;
+        if (okt) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              *reinterpret_cast<uint4*>(vrow + h * 16384 + ((cc ^ (i & 7)) << 4)) =
+                  make_uint4(0, 0, 0, 0);
+        }
+      }
+      const bool tail = pos > L;
+      bool need = false;
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) {
+        float v = x[n] * p.scale_log2;
+        if (!live || !((colbits >> n) & 1u)) v = -INFINITY;
+        if (tail && pos > L + tlim[n]) v = -INFINITY;
+        x[n] = v;
+        need |= v > m[n] + kRescaleSlack;
+      }
+      const int wvote = (__any_sync(0xffffffffu, need) ? 1 : 0) | (__any_sync(0xffffffffu, !okt) ? 2 : 0);
+      if (lane == 0) votes[grp * 4 + q4] = wvote;
+      named_bar(1 + grp, 128);
+      const int allv = votes[grp * 4] | votes[grp * 4 + 1] | votes[grp * 4 + 2] | votes[grp * 4 + 3];
+      if (allv & 2) {
+        ok = false;
+        break;
+      }
+      // The group's previous PV (tile t - 2) must have finished before its O^T
+      // is rescaled or its P^T buffer rewritten.
+      bool pv_ok = k == 0 || mbar_wait_bounded(pvdone(grp), (k - 1) & 1);
+      tc_fence_after();
+      if (allv & 1) {
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) {
+          float v = x[n];
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o2));
+          if (lane == 0) colmax[(grp * 4 + q4) * NQC + n] = v;
+        }
+        named_bar(1 + grp, 128);
+        float f[NQC];
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) {
+          const float* cm = colmax + grp * 4 * NQC;
+          const float mx = fmaxf(fmaxf(cm[n], cm[NQC + n]), fmaxf(cm[2 * NQC + n], cm[3 * NQC + n]));
+          const float mn = fmaxf(m[n], mx);
+          f[n] = ex2(m[n] - mn);
+          m[n] = mn;
+          ls[n] *= f[n];
+        }
+        if (k > 0 && pv_ok) {
+          // O^T row i of this group, columns scaled by f
+#pragma unroll
+          for (int c = 0; c < NQC / 8; ++c) {
+            float v8[8];
+            tmem_ld8(tl + o_col + 8 * c, v8);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v8[e] *= f[8 * c + e];
+            tmem_st8(tl + o_col + 8 * c, v8);
+          }
+          tmem_st_wait();
+        }
+        named_bar(1 + grp, 128);   // colmax is rewritten at the next rescale
+      }
+      // P^T operand, K-major with the 128-byte swizzle: element (n, i) at
+      // (i / 64) * NQP * 128 + n * 128 + (((i % 64) / 8) ^ (n % 8)) * 16 + (i % 8) * 2.
+      uint8_t* pbuf = smem + Cfg::kOffP + grp * Cfg::kP + (i >> 6) * (NQP * 128) + (i & 7) * 2;
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) {
+        const float pv = ex2(x[n] - m[n]);
+        ls[n] += pv;
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((((i & 63) >> 3) ^ (n & 7)) << 4)) =
+            __float2bfloat16_rn(pv);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(pready(grp));
+      if (!pv_ok) ok = false;   // the group leaves at the next vote
+      mytiles = k + 1;
+    }
+    // The group's last PV completes its O^T.
+    if (mytiles > 0 && !mbar_wait_bounded(pvdone(grp), (mytiles - 1) & 1)) ok = false;
+    tc_fence_after();
+    if (!ok && i == 0) set_error(p.err, kErrDeviceTimeout);
+
+    // Row sums over the group's 128 positions, then the two groups merge.
+#pragma unroll
+    for (int n = 0; n < NQC; ++n) {
+      float v = ls[n];
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+      if (lane == 0) colsum[(grp * 4 + q4) * NQC + n] = v;
+    }
+    named_bar(1 + grp, 128);
+    if (i < NQC) {
+      const float* cs = colsum + grp * 4 * NQC;
+      gm[grp * NQC + i] = m[i];
+      gl[grp * NQC + i] = (mytiles > 0) ? cs[i] + cs[NQC + i] + cs[2 * NQC + i] + cs[3 * NQC + i]
+                                        : 0.f;
+    }
+    named_bar(3, 256);
+    if (grp == 0) {
+      float o0[NQC], o1[NQC];
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) o0[n] = o1[n] = 0.f;
+      const bool has0 = ntiles > 0, has1 = ntiles > 1;
+      float v0[NQC / 8][8], v1[NQC / 8][8];
+#pragma unroll
+      for (int c = 0; c < NQC / 8; ++c) {
+        if (has0) tmem_ld8(tl + 64 + 8 * c, v0[c]);
+        if (has1) tmem_ld8(tl + 96 + 8 * c, v1[c]);
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < NQC / 8; ++c)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (has0) o0[8 * c + e] = v0[c][e];
+          if (has1) o1[8 * c + e] = v1[c][e];
+        }
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+      const size_t part = size_t(unit) * p.num_splits + split;
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) {
+        if (n < p.nq) {
+          const float m0 = gm[n], m1 = gm[NQC + n];
+          const float M = fmaxf(m0, m1);
+          const float f0 = has0 ? ex2(m0 - M) : 0.f, f1 = has1 ? ex2(m1 - M) : 0.f;
+          const float Ls = f0 * gl[n] + f1 * gl[NQC + n];
+          const float O = f0 * o0[n] + f1 * o1[n];
+          if (p.num_splits == 1) {
+            const int t = n / p.group, hl = n - t * p.group;
+            out[((size_t(b) * T + t) * p.hq + g * p.group + hl) * D + i] =
+                __float2bfloat16_rn(Ls > 0.f ? O / Ls : 0.f);
+          } else {
+            p.part_o[(part * p.nq + n) * D + i] = O;
+            if (i == n) {
+              p.part_ml[(part * p.nq + n) * 2 + 0] = M;
+              p.part_ml[(part * p.nq + n) * 2 + 1] = Ls;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+  if (p.num_splits > 1) {
+    SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    auto out_row = [&](int n) {
+      const int t = n / p.group, hl = n - t * p.group;
+      return out + ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D;
+    };
+    finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, p.nq, out_row,
+                                         reinterpret_cast<float*>(smem), flag);
+  }
+}
+
+template <int NQP, int NQC, bool CAP>
+static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const VerifyParams& p, int batch, cudaStream_t stream) {
+  using Cfg = TcCfg<NQP, NQC>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<NQP, NQC, CAP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(p.num_splits, p.hkv, batch);
+  verify_tc_kernel<NQP, NQC, CAP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+template <bool CAP>
+static cudaError_t launch_tc_cols(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                  const VerifyParams& p, int ncols, int batch, cudaStream_t s) {
+  switch ((ncols + 7) / 8) {
+    case 1: return launch_tc<16, 8, CAP>(kmap, vmap, p, batch, s);
+    case 2: return launch_tc<16, 16, CAP>(kmap, vmap, p, batch, s);
+    case 3: return launch_tc<32, 24, CAP>(kmap, vmap, p, batch, s);
+    case 4: return launch_tc<32, 32, CAP>(kmap, vmap, p, batch, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const VerifyParams& p, int ncols, bool capture, int batch,
+                             cudaStream_t stream) {
+  return capture ? launch_tc_cols<true>(kmap, vmap, p, ncols, batch, stream)
+                 : launch_tc_cols<false>(kmap, vmap, p, ncols, batch, stream);
+}
+
+}  // namespace vegas

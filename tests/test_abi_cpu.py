@@ -66,7 +66,7 @@ def test_host_validation_rejects_before_launch(vg):
     assert ei.value.status == 2
     kv = vg.PagedKV(16, 16, 16, 1, 16, 8, 2, 96, 1)     # head_dim 96
     with pytest.raises(vg.VegasError) as ei:
-        vg.vegas_sparse_decode_attn(kv, 16, 16, 16, 4, 16, 16, 16, 1, 1, 0.1, None, 0, stream=0)
+        vg.vegas_sparse_decode_attn(kv, 16, 16, 16, 4, 16, 16, 16, 1, 1, 0.1, stream=0)
     assert ei.value.status == 2
     kv = vg.PagedKV(16, 16, 16, 1, 16, 64, 2, 128, 1)   # (gamma+1)*G = 5*32 rows
     with pytest.raises(vg.VegasError) as ei:

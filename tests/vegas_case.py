@@ -99,10 +99,8 @@ class Case:
         tl_t = torch.full((w.batch,), tl, dtype=torch.int32, device=DEV)
         q = self.qd[step] if q is None else q
         out = torch.empty_like(q)
-        nbytes = vg.vegas_sparse_workspace_size(self.kv, w.batch, k_max, tl)
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=DEV)
         vg.vegas_sparse_decode_attn(self.kv, q, out, idx, k_max, kps_t, self.lens_t, tl_t, tl,
-                                    w.batch, self.scale, ws, ws.numel())
+                                    w.batch, self.scale)
         return out
 
     # ------------------------------------------------------------ oracle view
