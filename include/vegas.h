@@ -135,7 +135,7 @@ vegas_status_t vegas_verify_attn_capture_noalloc(
  * out_idx[(b * num_kv_heads + g) * k_max + j], j < k_b; entries j >= k_b are
  * set to -1.  -0.0 ranks equal to +0.0.  NaN scores are outside the
  * contract (they rank lowest).  Needs 0 <= k_b <= min(L_b, k_max) and
- * L_b <= score_stride <= 524288.
+ * L_b <= score_stride <= 262144.
  * ---------------------------------------------------------------------- */
 vegas_status_t vegas_select_topk(
     const float* scores, int score_stride, const int32_t* ctx_lens,

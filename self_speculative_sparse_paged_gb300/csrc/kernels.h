@@ -60,7 +60,7 @@ struct SelectParams {
   int score_stride;
   int hkv;
   int k_max;
-  int chunk;                // keys per CTA of a cluster
+  int chunk;                // keys per CTA of a cluster, a multiple of select_chunk_quantum()
   int* err;
 };
 
@@ -87,6 +87,7 @@ cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int b
                           cudaStream_t stream);
 
 int select_max_chunk();
+int select_chunk_quantum();   // a CTA's chunk is a multiple of this
 cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream);
 
 cudaError_t launch_synth_kv(void* cache, int which, uint64_t seed, int layer, const int32_t* owner,

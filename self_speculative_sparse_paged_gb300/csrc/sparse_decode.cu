@@ -219,24 +219,37 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   // memory, M = max_r m_r, w_r = 2^(m_r - M) / sum_r 2^(m_r - M) l_r.
   cluster.sync();
   if (rank == 0) {
+    constexpr int R = kMaxSparseCluster;   // remote loads are issued together, unrolled
     for (int n = tid; n < p.group; n += NTH) {
+      float mr[R], lr[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        mr[r] = r < CL ? cluster.map_shared_rank(pM, r)[n] : -INFINITY;
+        lr[r] = r < CL ? cluster.map_shared_rank(pL, r)[n] : 0.f;
+      }
       float M = -INFINITY;
-      for (int r = 0; r < CL; ++r) M = fmaxf(M, cluster.map_shared_rank(pM, r)[n]);
+#pragma unroll
+      for (int r = 0; r < R; ++r) M = fmaxf(M, mr[r]);
       float L = 0.f;
-      for (int r = 0; r < CL; ++r) {
-        const float f = ex2(cluster.map_shared_rank(pM, r)[n] - M);
-        wts[r * NPAD + n] = f;
-        L += f * cluster.map_shared_rank(pL, r)[n];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        mr[r] = r < CL ? ex2(mr[r] - M) : 0.f;
+        L += mr[r] * lr[r];
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      for (int r = 0; r < CL; ++r) wts[r * NPAD + n] *= inv;
+#pragma unroll
+      for (int r = 0; r < R; ++r) wts[r * NPAD + n] = mr[r] * inv;
     }
     __syncthreads();
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     for (int e = tid; e < p.group * D; e += NTH) {
       const int n = e / D;
+      float v[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) v[r] = r < CL ? cluster.map_shared_rank(pO, r)[e] : 0.f;
       float a = 0.f;
-      for (int r = 0; r < CL; ++r) a += wts[r * NPAD + n] * cluster.map_shared_rank(pO, r)[e];
+#pragma unroll
+      for (int r = 0; r < R; ++r) a += wts[r * NPAD + n] * v[r];
       out[(size_t(b) * p.hq + g * p.group + n) * D + (e % D)] = __float2bfloat16_rn(a);
     }
   }

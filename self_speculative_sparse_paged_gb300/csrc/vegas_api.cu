@@ -323,17 +323,23 @@ VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride
     return fail(VEGAS_ERR_INVALID_ARG, "batch %d, num_kv_heads %d, k_max %d, score_stride %d",
                 batch, num_kv_heads, k_max, score_stride);
   const int max_chunk = vegas::select_max_chunk();
-  if ((long long)score_stride > 16ll * max_chunk)
-    return fail(VEGAS_ERR_UNSUPPORTED, "score_stride %d exceeds %d", score_stride, 16 * max_chunk);
+  if ((long long)score_stride > 8ll * max_chunk)
+    return fail(VEGAS_ERR_UNSUPPORTED, "score_stride %d exceeds %d", score_stride, 8 * max_chunk);
   if (batch == 0 || k_max == 0) return VEGAS_OK;
   int* err = nullptr;
   int sms = 0;
   vegas_status_t st = device_info(&err, &sms);
   if (st != VEGAS_OK) return st;
   const int units = batch * num_kv_heads;
+  const int quantum = vegas::select_chunk_quantum();
+  auto chunk_for = [&](int c) {
+    const int ch = (score_stride + c - 1) / c;
+    return (ch + quantum - 1) / quantum * quantum;
+  };
   int cl = 1;
-  while ((score_stride + cl - 1) / cl > max_chunk) cl *= 2;
-  while (cl < 8 && units * cl * 2 <= sms && (score_stride + 2 * cl - 1) / (2 * cl) >= 1024) cl *= 2;
+  while (chunk_for(cl) > max_chunk) cl *= 2;
+  // spread small batches over more CTAs while each keeps a full quantum of keys
+  while (cl < 8 && units * cl * 2 <= sms && score_stride / (2 * cl) >= quantum) cl *= 2;
   vegas::SelectParams p{};
   p.scores = scores;
   p.ctx_lens = ctx_lens;
@@ -342,7 +348,7 @@ VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride
   p.score_stride = score_stride;
   p.hkv = num_kv_heads;
   p.k_max = k_max;
-  p.chunk = (score_stride + cl - 1) / cl;
+  p.chunk = chunk_for(cl);
   p.err = err;
   cudaError_t e = vegas::launch_select(p, cl, batch, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "select launch");
