@@ -27,6 +27,7 @@ struct VerifyParams {
   float scale_log2;         // scale * log2(e)
   int pages_per_split;
   int num_splits;
+  int cluster_merge;        // tcgen05 kernel: the splits of a unit form one cluster and merge on chip
   int* tickets;
   float* part_ml;
   float* part_o;
@@ -71,13 +72,16 @@ int record_failure(int status, const char* msg);
 
 // Largest 8-row query tile count per head_dim (d=128: 48 rows, d=64: 64 rows).
 inline int verify_max_ntiles(int head_dim) { return head_dim == 128 ? 6 : 8; }
-// tcgen05 verify kernel (head_dim 128, at most 32 query columns incl. capture);
-// its splits must cover whole 8-page tiles.
+// tcgen05 verify kernel (head_dim 128, at most 32 query columns incl. capture),
+// streaming 8-page tiles.
 constexpr int kTcMaxColumns = 32;
 constexpr int kTcPagesPerTile = 8;
+constexpr int kMaxVerifyCluster = 16;   // splits merged on chip (non-portable cluster size)
 cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const VerifyParams& p, int ncols, bool capture, int batch,
                              cudaStream_t stream);
+// Clusters of `cluster` CTAs of the tcgen05 kernel resident at once (0: none / error).
+int verify_tc_max_active_clusters(int ncols, bool capture, int cluster);
 template <int D, bool CAP>
 cudaError_t launch_verify_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
                             const VerifyParams& p, int ntiles, int batch, cudaStream_t stream);

@@ -61,11 +61,6 @@ vegas_status_t device_info(int** err, int* sms) {
   return VEGAS_OK;
 }
 
-int current_sms() {
-  int sms = 0;
-  if (device_info(nullptr, &sms) != VEGAS_OK || sms <= 0) sms = 148;
-  return sms;
-}
 
 // ----------------------------------------------------------------- TMA maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -157,7 +152,8 @@ int verify_splits(int units, int max_pages, int sms) {
 
 struct VerifyPlan {
   int nq, ncols, ntiles, splits, pages_per_split;
-  bool tc;   // tcgen05 kernel (head_dim 128, <= 32 columns) instead of the mma.sync one
+  bool tc;        // tcgen05 kernel (head_dim 128, <= 32 columns) instead of the mma.sync one
+  bool cluster;   // tcgen05 kernel with the splits of a unit in one cluster: no workspace
   size_t tickets_off, ml_off, o_off, bytes;
 };
 
@@ -165,8 +161,8 @@ struct VerifyPlan {
 // two columns holding the summed captured query (at the next even index).
 int verify_columns(int nq, bool capture) { return capture ? ((nq + 1) & ~1) + 2 : nq; }
 
-VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms,
-                       bool capture = true) {
+VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms, bool capture,
+                       bool with_device) {
   VerifyPlan pl{};
   const int G = kv->num_q_heads / kv->num_kv_heads;
   pl.nq = (gamma + 1) * G;
@@ -174,6 +170,19 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
   pl.ntiles = (pl.ncols + 7) / 8;
   pl.tc = kv->head_dim == 128 && pl.ncols <= vegas::kTcMaxColumns;
   const int units = std::max(1, batch * kv->num_kv_heads);
+  if (pl.tc && units < sms && with_device) {
+    // One cluster per unit, every CTA resident (one wave), >= one tile per split;
+    // the splits merge through distributed shared memory.
+    int S = std::min(std::min(vegas::kMaxVerifyCluster, sms / units),
+                     std::max(1, kv->max_pages_per_seq / vegas::kTcPagesPerTile));
+    while (S > 1 && vegas::verify_tc_max_active_clusters(pl.ncols, capture, S) < units) --S;
+    if (S > 1) {
+      pl.pages_per_split = (kv->max_pages_per_seq + S - 1) / S;
+      pl.splits = (kv->max_pages_per_seq + pl.pages_per_split - 1) / pl.pages_per_split;
+      pl.cluster = true;
+      return pl;   // bytes = 0
+    }
+  }
   pl.splits = verify_splits(units, kv->max_pages_per_seq, sms);
   pl.pages_per_split = (kv->max_pages_per_seq + pl.splits - 1) / pl.splits;
   // splits cover whole tiles: 8 pages (tcgen05 kernel) or page pairs
@@ -232,9 +241,11 @@ int record_failure(int status, const char* msg) {
 // =========================================================================
 VEGAS_API size_t vegas_verify_workspace_size(const vegas_paged_kv_t* kv, int batch, int gamma) {
   if (check_kv(kv) != VEGAS_OK || batch < 0 || gamma < 0) return 0;
-  const int sms = current_sms();
-  return std::max(plan_verify(kv, batch, gamma, sms, true).bytes,
-                  plan_verify(kv, batch, gamma, sms, false).bytes);
+  int sms = 0;
+  const bool dev = device_info(nullptr, &sms) == VEGAS_OK && sms > 0;
+  if (!dev) sms = 148;
+  return std::max(plan_verify(kv, batch, gamma, sms, true, dev).bytes,
+                  plan_verify(kv, batch, gamma, sms, false, dev).bytes);
 }
 
 VEGAS_API vegas_status_t vegas_verify_attn_capture(
@@ -265,8 +276,8 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   int* err = nullptr;
   int sms = 0;
   if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
-  const VerifyPlan pl = plan_verify(kv, batch, gamma, sms, scores != nullptr);
-  if (pl.splits > 1) {
+  const VerifyPlan pl = plan_verify(kv, batch, gamma, sms, scores != nullptr, true);
+  if (pl.splits > 1 && !pl.cluster) {
     if (!workspace || workspace_bytes < pl.bytes)
       return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "verify workspace %zu < %zu bytes",
                   workspace_bytes, pl.bytes);
@@ -296,6 +307,7 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.pages_per_split = pl.pages_per_split;
   p.num_splits = pl.splits;
+  p.cluster_merge = pl.cluster ? 1 : 0;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.tickets = ws ? reinterpret_cast<int*>(ws + pl.tickets_off) : nullptr;
   p.part_ml = ws ? reinterpret_cast<float*>(ws + pl.ml_off) : nullptr;

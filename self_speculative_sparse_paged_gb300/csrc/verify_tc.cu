@@ -25,8 +25,12 @@
 // 8 (one vote per group); only then is the group's O^T rescaled in tensor
 // memory.  It writes P^T = 2^(x - m) as bf16 into a 128-byte-swizzled shared
 // buffer that the PV MMA reads.
+#include <cooperative_groups.h>
+
 #include "kernels.h"
 #include "split_merge.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace vegas {
 
@@ -34,13 +38,14 @@ template <int NQP, int NQC>
 struct TcCfg {
   static constexpr int D = 128;
   // K and V tiles live in separate rings: a K slot frees when its S MMA
-  // completes, a V slot only when its PV MMA does, so V gets the deeper ring.
-  static constexpr int KS = 2;
-  static constexpr int VS = 4;
+  // completes, a V slot only when its PV MMA does.  Under full HBM load a
+  // tile's load latency reaches ~2 us, which each ring must cover on its own.
+  static constexpr int KS = 3;
+  static constexpr int VS = 3;
   static constexpr int kKV = 128 * D * 2;            // one K (or V) tile, 32 KB
   static constexpr int kQ = 2 * NQP * 128;           // Q^T operand [half][NQP][128 B]
   static constexpr int kP = 2 * NQP * 128;           // P^T operand [kblock][NQP][128 B]
-  static constexpr int kThreads = 352;               // 11 warps
+  static constexpr int kThreads = 384;               // 12 warps
   static constexpr uint32_t kTmemCols = 128;         // S0, S1, O0, O1 at columns 0, 32, 64, 96
   static constexpr int kOffV = KS * kKV;
   static constexpr int kOffQ = (KS + VS) * kKV;
@@ -54,8 +59,63 @@ struct TcCfg {
   static constexpr size_t kSmem = size_t(kOffMisc) + kMisc + 1024;
 };
 
+// Split-KV merge on chip, when the num_splits CTAs of a (sequence, KV head)
+// unit form one thread-block cluster (rank = split).  Each CTA has staged its
+// state in shared memory at `st`: O[n][d] (unnormalised, NQC x 128), then
+// M[NQC] (running maxima, log2 units) and L[NQC] (row sums).  After a cluster
+// barrier, CTA r merges rows n = r, r + S, ... reading the S states through
+// distributed shared memory (merge rule as in split_merge.cuh), writes bf16
+// rows, and leaves only once no CTA reads its shared memory any more.  Called
+// by every thread of every CTA of the cluster.
+template <int NQC, class OutRow>
+__device__ __forceinline__ void cluster_merge_rows(const float* st, int S, int nq, OutRow out_row) {
+  constexpr int D = 128;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int r = (int)cluster.block_rank(), tid = threadIdx.x;
+  if (tid < 2 * D) {
+    const int d = tid & (D - 1);
+    for (int n = r + (tid >> 7) * S; n < nq; n += 2 * S) {
+      // eight splits' loads in flight at a time, merged into a running state
+      float M = kEmptyMax, Lsum = 0.f, O = 0.f;
+      for (int s0 = 0; s0 < S; s0 += 8) {
+        float ms[8], ls[8], os[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (s0 + j < S) {
+            const float* rs = cluster.map_shared_rank(st, s0 + j);
+            os[j] = rs[n * D + d];
+            ms[j] = rs[NQC * D + n];
+            ls[j] = rs[NQC * D + NQC + n];
+          } else {
+            os[j] = ls[j] = 0.f;
+            ms[j] = kEmptyMax;
+          }
+        }
+        float Mn = M;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, ms[j]);
+        const float f = ex2(M - Mn);
+        Lsum *= f;
+        O *= f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float fj = ex2(ms[j] - Mn);
+          Lsum += fj * ls[j];
+          O += fj * os[j];
+        }
+        M = Mn;
+      }
+      out_row(n)[d] = __float2bfloat16_rn(Lsum > 0.f ? O / Lsum : 0.f);
+    }
+  }
+  // no CTA leaves while another may still read its shared memory
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 template <int NQP, int NQC, bool CAPTURE>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const VerifyParams p) {
   using Cfg = TcCfg<NQP, NQC>;
@@ -183,93 +243,135 @@ __global__ void __launch_bounds__(352, 1)
   }
   bool ok = true;
 
-  if (warp == 0 || warp == 10) {
+  if (warp == 0 || warp >= 10) {
     // ------------------------------------------------------------ producers
-    // warp 0 streams the K tiles, warp 10 the V tiles, each through its ring;
-    // lanes 0..7 load one page (two 64-column boxes) of the tile each.
-    const bool is_k = warp == 0;
+    // TMA issue rate is per warp, so a tile's 32 boxes (8 pages x 2 column
+    // halves, of K and of V) are spread over three warps, in half-warps:
+    //   warp 0,  lanes 0-15:  K pages 0-5, arms the K slot's barrier;
+    //   warp 10, lanes 0-15:  V pages 0-5, arms the V slot's barrier;
+    //   warp 11, lanes 0-15:  K pages 6-7;  lanes 16-31: V pages 6-7.
+    // Lane j < np of a half-warp loads page pf + j (two 64-column boxes).
+    const int half = lane >> 4, hl = lane & 15;
+    const unsigned hmask = 0xFFFFu << (16 * half);
+    const bool active = warp == 11 || half == 0;
+    const bool is_k = warp == 11 ? half == 0 : warp == 0;
+    const bool arms = warp != 11;
+    const int pf = warp == 11 ? 6 : 0, np = warp == 11 ? 2 : 6;
     const int depth = is_k ? KS : VS;
     const CUtensorMap* map = is_k ? &kmap : &vmap;
     const uint32_t ring = sbase + (is_k ? 0 : Cfg::kOffV);
     const int32_t* bt_row = p.block_table + size_t(b) * p.max_pages;
+    // Block-table entries are prefetched four tiles ahead, one register per
+    // tile modulo 4, so a load is consumed four iterations after its issue.
+    auto table_entry = [&](int tt) {
+      int page = pbeg + 8 * tt + pf + hl;
+      if (page >= pend) page = pbeg + 8 * tt;         // loaded again, masked by the softmax
+      return (hl < np && tt < ntiles) ? __ldg(&bt_row[page]) : 0;
+    };
     int issued = 0;
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const int s = t % depth;
-      const uint32_t full = is_k ? kfull(s) : vfull(s);
-      const uint32_t freed = is_k ? kfree(s) : vfree(s);
-      if (t >= depth && !mbar_wait_bounded(freed, ((t / depth) - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      int page = pbeg + 8 * t + (lane & 7);
-      if (page >= pend) page = pbeg + 8 * t;          // loaded again, masked by the softmax
-      int phys = lane < 8 ? __ldg(&bt_row[page]) : 0;
-      if (lane < 8 && (phys < 0 || phys >= p.num_pages)) {
-        set_error(p.err, kErrDeviceFault);
-        phys = 0;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(full, Cfg::kKV);
-      __syncwarp();
-      if (lane < 8) {
-        const int row = (phys * p.hkv + g) * 16;
-        const uint32_t dst = ring + s * Cfg::kKV + lane * 2048;
-        tma_load_2d(dst, map, 0, row, full);
-        tma_load_2d(dst + 16384, map, 64, row, full);
-      }
-      __syncwarp();
-      issued = t + 1;
-    }
-    if (!ok) {
-      if (lane == 0) set_error(p.err, kErrDeviceTimeout);
-      for (int t = max(0, issued - depth); t < issued; ++t)
-        (void)mbar_wait_bounded(is_k ? kfull(t % depth) : vfull(t % depth), (t / depth) & 1);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, NQP, 0, 0);
-      constexpr uint32_t idPV = idesc_bf16(128, NQP, 1, 0);
-      auto issue_pv = [&](int t) -> bool {
-        const int gg = t & 1, s = t % VS;
-        if (!mbar_wait_bounded(pready(gg), (t >> 1) & 1)) return false;
-        if (!mbar_wait_bounded(vfull(s), (t / VS) & 1)) return false;
-        tc_fence_after();
-        const uint32_t vb = sbase + Cfg::kOffV + s * Cfg::kKV;
-        const uint32_t pb = sbase + Cfg::kOffP + gg * Cfg::kP;
+    if (active) {
+      int held[4];
 #pragma unroll
-        for (int kp = 0; kp < 8; ++kp) {
-          const uint64_t a = smem_desc(vb + kp * 2048, 16384, 1024, 2);
-          const uint64_t bd = smem_desc(pb + (kp >> 2) * (NQP * 128) + (kp & 3) * 32, 16, 1024, 2);
-          tc_mma(tmem + 64 + 32 * gg, a, bd, idPV, t >= 2 || kp > 0);
-        }
-        tc_commit(pvdone(gg));
-        tc_commit(vfree(s));
-        return true;
-      };
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int s = t % KS, gg = t & 1;
-        if (!mbar_wait_bounded(kfull(s), (t / KS) & 1)) { ok = false; break; }
-        if (t >= 2 && !mbar_wait_bounded(sread(gg), ((t >> 1) - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kb = sbase + s * Cfg::kKV;
-        const uint32_t qb = sbase + Cfg::kOffQ;
+      for (int j = 0; j < 4; ++j) held[j] = table_entry(j);
+      for (int t0 = 0; t0 < ntiles && ok; t0 += 4) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a = smem_desc(kb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2);
-          const uint64_t bd = smem_desc(qb + (ks >> 2) * (NQP * 128) + (ks & 3) * 32, 16, 1024, 2);
-          tc_mma(tmem + 32 * gg, a, bd, idS, ks > 0);
+        for (int j = 0; j < 4; ++j) {
+          const int t = t0 + j;
+          if (t >= ntiles) break;
+          const int s = t % depth;
+          const uint32_t full = is_k ? kfull(s) : vfull(s);
+          const uint32_t freed = is_k ? kfree(s) : vfree(s);
+          // the half-warp agrees on the outcome, so it leaves together
+          if (t >= depth &&
+              !__all_sync(hmask, mbar_wait_bounded(freed, ((t / depth) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          int phys = held[j];
+          held[j] = table_entry(t + 4);
+          if (hl < np && (phys < 0 || phys >= p.num_pages)) {
+            set_error(p.err, kErrDeviceFault);
+            phys = 0;
+          }
+          // one arrival per phase, with the whole tile's bytes; the other
+          // half-warp's loads count against it
+          if (arms && hl == 0) mbar_arrive_expect_tx(full, Cfg::kKV);
+          __syncwarp(hmask);
+          if (hl < np) {
+            const int row = (phys * p.hkv + g) * 16;
+            const uint32_t dst = ring + s * Cfg::kKV + (pf + hl) * 2048;
+            tma_load_2d(dst, map, 0, row, full);
+            tma_load_2d(dst + 16384, map, 64, row, full);
+          }
+          __syncwarp(hmask);
+          issued = t + 1;
         }
-        tc_commit(sfull(gg));
-        tc_commit(kfree(s));
-        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
       }
-      if (ok && ntiles > 0 && !issue_pv(ntiles - 1)) ok = false;
-      if (!ok) set_error(p.err, kErrDeviceTimeout);
-      // every MMA issued has completed before tensor memory is released
-      tc_commit(drain);
-      (void)mbar_wait_bounded(drain, 0);
+      if (!ok) {
+        if (hl == 0) set_error(p.err, kErrDeviceTimeout);
+        for (int t = max(0, issued - depth); t < issued; ++t)
+          (void)mbar_wait_bounded(is_k ? kfull(t % depth) : vfull(t % depth), (t / depth) & 1);
+      }
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop, so its control flow and the operand
+    // descriptors stay warp-uniform; one elected lane issues and commits.
+    constexpr uint32_t idS = idesc_bf16(128, NQP, 0, 0);
+    constexpr uint32_t idPV = idesc_bf16(128, NQP, 1, 0);
+    const bool leader = elect_one();
+    // Descriptors without their start address; the address field (bits 0-13)
+    // holds (address / 16) mod 2^14, the part of a shared-window address the
+    // tensor cores use, so it is added and masked last.
+    const uint64_t dSw = smem_desc(0, 16, 1024, 2);       // K-major, 128-byte swizzle
+    const uint64_t dVmn = smem_desc(0, 16384, 1024, 2);   // V as the MN-major A operand
+    auto with_addr = [](uint64_t d, uint32_t a16) { return d | uint64_t(a16 & 0x3FFFu); };
+    const uint32_t qb = (sbase + Cfg::kOffQ) >> 4;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+    };
+    auto issue_pv = [&](int t) -> bool {
+      const int gg = t & 1, s = t % VS;
+      if (!wait_all(pready(gg), (t >> 1) & 1)) return false;
+      if (!wait_all(vfull(s), (t / VS) & 1)) return false;
+      tc_fence_after();
+      const uint32_t vb = (sbase + Cfg::kOffV + s * Cfg::kKV) >> 4;
+      const uint32_t pb = (sbase + Cfg::kOffP + gg * Cfg::kP) >> 4;
+      if (leader) {
+#pragma unroll
+        for (int kp = 0; kp < 8; ++kp)
+          tc_mma(tmem + 64 + 32 * gg, with_addr(dVmn, vb + kp * 128),
+                 with_addr(dSw, pb + (kp >> 2) * (NQP * 8) + (kp & 3) * 2), idPV, t >= 2 || kp > 0);
+        tc_commit(pvdone(gg));
+        tc_commit(vfree(s));
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int s = t % KS, gg = t & 1;
+      if (!wait_all(kfull(s), (t / KS) & 1)) { ok = false; break; }
+      if (t >= 2 && !wait_all(sread(gg), ((t >> 1) - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t kb = (sbase + s * Cfg::kKV) >> 4;
+      if (leader) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma(tmem + 32 * gg, with_addr(dSw, kb + (ks >> 2) * 1024 + (ks & 3) * 2),
+                 with_addr(dSw, qb + (ks >> 2) * (NQP * 8) + (ks & 3) * 2), idS, ks > 0);
+        tc_commit(sfull(gg));
+        tc_commit(kfree(s));
+      }
+      __syncwarp();
+      if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+    }
+    if (ok && ntiles > 0 && !issue_pv(ntiles - 1)) ok = false;
+    if (!ok && leader) set_error(p.err, kErrDeviceTimeout);
+    // every MMA issued has completed before tensor memory is released
+    if (leader) tc_commit(drain);
+    __syncwarp();
+    (void)mbar_wait_bounded(drain, 0);
   } else {
     // ------------------------------------------------------------ softmax groups (warps 2-9)
     const int grp = (warp - 2) >> 2;          // 0: even tiles, 1: odd tiles
@@ -453,18 +555,34 @@ __global__ void __launch_bounds__(352, 1)
         }
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
       const size_t part = size_t(unit) * p.num_splits + split;
+      // All shared-memory reads and the merge arithmetic first, the stores
+      // after: interleaved, every store would order the next column's loads.
+      float Mv[NQC], Lv[NQC];
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) {
+        const float m0 = gm[n], m1 = gm[NQC + n];
+        const float M = fmaxf(m0, m1);
+        const float f0 = has0 ? ex2(m0 - M) : 0.f, f1 = has1 ? ex2(m1 - M) : 0.f;
+        Mv[n] = M;
+        Lv[n] = f0 * gl[n] + f1 * gl[NQC + n];
+        o0[n] = f0 * o0[n] + f1 * o1[n];
+      }
 #pragma unroll
       for (int n = 0; n < NQC; ++n) {
         if (n < p.nq) {
-          const float m0 = gm[n], m1 = gm[NQC + n];
-          const float M = fmaxf(m0, m1);
-          const float f0 = has0 ? ex2(m0 - M) : 0.f, f1 = has1 ? ex2(m1 - M) : 0.f;
-          const float Ls = f0 * gl[n] + f1 * gl[NQC + n];
-          const float O = f0 * o0[n] + f1 * o1[n];
+          const float M = Mv[n], Ls = Lv[n], O = o0[n];
           if (p.num_splits == 1) {
             const int t = n / p.group, hl = n - t * p.group;
             out[((size_t(b) * T + t) * p.hq + g * p.group + hl) * D + i] =
                 __float2bfloat16_rn(Ls > 0.f ? O / Ls : 0.f);
+          } else if (p.cluster_merge) {
+            // this split's state for the cluster merge; the Q and P buffers are free now
+            float* stO = reinterpret_cast<float*>(smem + Cfg::kOffQ);
+            stO[n * D + i] = O;
+            if (i == n) {
+              stO[NQC * D + n] = M;
+              stO[NQC * D + NQC + n] = Ls;
+            }
           } else {
             p.part_o[(part * p.nq + n) * D + i] = O;
             if (i == n) {
@@ -484,20 +602,24 @@ __global__ void __launch_bounds__(352, 1)
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
   if (p.num_splits > 1) {
-    SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     auto out_row = [&](int n) {
       const int t = n / p.group, hl = n - t * p.group;
       return out + ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D;
     };
-    finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, p.nq, out_row,
-                                         reinterpret_cast<float*>(smem), flag);
+    if (p.cluster_merge) {
+      cluster_merge_rows<NQC>(reinterpret_cast<const float*>(smem + Cfg::kOffQ), p.num_splits,
+                              p.nq, out_row);
+    } else {
+      SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
+      finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, p.nq, out_row,
+                                           reinterpret_cast<float*>(smem), flag);
+    }
   }
 }
 
 template <int NQP, int NQC, bool CAP>
-static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             const VerifyParams& p, int batch, cudaStream_t stream) {
+static cudaError_t configure_tc() {
   using Cfg = TcCfg<NQP, NQC>;
   static bool configured = false;
   if (!configured) {
@@ -505,21 +627,48 @@ static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(verify_tc_kernel<NQP, NQC, CAP>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(p.num_splits, p.hkv, batch);
-  verify_tc_kernel<NQP, NQC, CAP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  return cudaSuccess;
+}
+
+// Launch (launch = true) or, with launch = false, the number of clusters of
+// p.num_splits CTAs that can be resident at once (into *clusters).
+template <int NQP, int NQC, bool CAP>
+static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const VerifyParams& p, int batch, cudaStream_t stream, bool launch,
+                             int* clusters) {
+  using Cfg = TcCfg<NQP, NQC>;
+  cudaError_t e = configure_tc<NQP, NQC, CAP>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits, p.hkv, batch);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cluster_merge ? p.num_splits : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!launch) return cudaOccupancyMaxActiveClusters(clusters, verify_tc_kernel<NQP, NQC, CAP>, &cfg);
+  return cudaLaunchKernelEx(&cfg, verify_tc_kernel<NQP, NQC, CAP>, kmap, vmap, p);
 }
 
 template <bool CAP>
 static cudaError_t launch_tc_cols(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                  const VerifyParams& p, int ncols, int batch, cudaStream_t s) {
+                                  const VerifyParams& p, int ncols, int batch, cudaStream_t s,
+                                  bool launch, int* clusters) {
   switch ((ncols + 7) / 8) {
-    case 1: return launch_tc<16, 8, CAP>(kmap, vmap, p, batch, s);
-    case 2: return launch_tc<16, 16, CAP>(kmap, vmap, p, batch, s);
-    case 3: return launch_tc<32, 24, CAP>(kmap, vmap, p, batch, s);
-    case 4: return launch_tc<32, 32, CAP>(kmap, vmap, p, batch, s);
+    case 1: return launch_tc<16, 8, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    case 2: return launch_tc<16, 16, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    case 3: return launch_tc<32, 24, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    case 4: return launch_tc<32, 32, CAP>(kmap, vmap, p, batch, s, launch, clusters);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -527,8 +676,32 @@ static cudaError_t launch_tc_cols(const CUtensorMap& kmap, const CUtensorMap& vm
 cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const VerifyParams& p, int ncols, bool capture, int batch,
                              cudaStream_t stream) {
-  return capture ? launch_tc_cols<true>(kmap, vmap, p, ncols, batch, stream)
-                 : launch_tc_cols<false>(kmap, vmap, p, ncols, batch, stream);
+  return capture ? launch_tc_cols<true>(kmap, vmap, p, ncols, batch, stream, true, nullptr)
+                 : launch_tc_cols<false>(kmap, vmap, p, ncols, batch, stream, true, nullptr);
+}
+
+int verify_tc_max_active_clusters(int ncols, bool capture, int cluster) {
+  if (cluster < 1 || cluster > kMaxVerifyCluster) return 0;
+  static int cache[2][5][kMaxVerifyCluster + 1];   // [capture][column tiles][cluster]
+  const int ct = (ncols + 7) / 8;
+  if (ct < 1 || ct > 4) return 0;
+  int& c = cache[capture ? 1 : 0][ct][cluster];
+  if (c == 0) {
+    VerifyParams p{};
+    p.hkv = 1;
+    p.num_splits = cluster;
+    p.cluster_merge = 1;
+    CUtensorMap none{};
+    int n = 0;
+    cudaError_t e = capture ? launch_tc_cols<true>(none, none, p, ncols, 1, 0, false, &n)
+                            : launch_tc_cols<false>(none, none, p, ncols, 1, 0, false, &n);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
 }
 
 }  // namespace vegas

@@ -7,6 +7,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import oracle  # noqa: E402
+import self_speculative_sparse_paged_gb300 as vg  # noqa: E402
 from vegas_case import Case, assert_attention_close, bf16_to_f64, score_bound  # noqa: E402
 from workload import configs  # noqa: E402
 
@@ -28,7 +29,9 @@ SMALL = {
     "gptoss_gamma6_g9": C4.with_(batch=1, hq=72, hkv=8, gamma=5, ctx_lo=900, ctx_hi=900),  # 54 rows
     "mha_g1": T.with_(hq=4, hkv=4, gamma=3, ctx_lo=600, ctx_hi=600),
     "odd_rows_g3": C4.with_(batch=1, hq=24, hkv=8, gamma=4, ctx_lo=500, ctx_hi=500),
-    "long_split": C2.with_(ctx_lo=20000, ctx_hi=20000, hkv=2, hq=8),
+    "long_split": C2.with_(ctx_lo=20000, ctx_hi=20000, hkv=2, hq=8),       # 16-CTA clusters
+    "cluster3_ragged": C2.with_(ctx_lo=400, ctx_hi=400),                   # 3 splits of 9, 9, 8 pages
+    "qwen_b2_mixed": C3.with_(batch=2, ctx_lo=150, ctx_hi=6000),           # one short, one long
 }
 
 
@@ -91,3 +94,18 @@ def test_repeat_calls_are_deterministic():
     o2, s2 = c.verify()
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert torch.equal(s1, s2)
+
+
+def test_cluster_merged_shape_needs_no_workspace():
+    # 8 (sequence, KV head) units at head_dim 128: the splits merge on chip
+    c = Case(C2.with_(ctx_lo=5000, ctx_hi=5000), device_gen=True)
+    w = c.w
+    assert vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma) == 0
+    ref_out, ref_scores = c.verify()
+    out = torch.empty_like(c.qv)
+    scores = torch.full_like(ref_scores, float("nan"))
+    vg.vegas_verify_attn_capture(c.kv, c.qv, out, scores, c.stride, c.lens_t, w.batch, w.gamma,
+                                 0, w.gamma, c.scale, None, 0)
+    vg.vegas_read_device_status()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(scores[..., :5000], ref_scores[..., :5000])

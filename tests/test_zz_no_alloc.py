@@ -30,10 +30,12 @@ def _noalloc(c: Case):
     return out, scores
 
 
+# Shapes whose split-KV merge goes through the scratch (the mma.sync kernel:
+# head_dim 64, or more than 32 query columns at head_dim 128).
 @pytest.mark.parametrize("w", [
-    configs.QWEN3_8B_B1_32K.with_(ctx_lo=20000, ctx_hi=20000),
-    configs.QWEN3_8B_B8_48K_64K.with_(batch=3, ctx_lo=3000, ctx_hi=9000),
-], ids=["qwen_b1", "qwen_b3"])
+    configs.GPTOSS_20B_B4_128K.with_(batch=1, ctx_lo=20000, ctx_hi=20000),
+    configs.QWEN3_8B_B8_48K_64K.with_(batch=3, ctx_lo=3000, ctx_hi=9000, gamma=8),
+], ids=["gptoss_b1", "qwen_b3_gamma8"])
 def test_noalloc_matches_workspace_entry_point_twice(w):
     c = Case(w, device_gen=True)
     assert 0 < vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma) <= \
