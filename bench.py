@@ -233,8 +233,15 @@ def run_gpu(args, rank, world, dist):
         evs = make_events(torch, chunk, True)
     except TypeError:
         evs = None
+    # The timed graph has no event nodes between the kernels, so each kernel
+    # may launch while its predecessor drains (programmatic dependent launch);
+    # a second graph with events at the stage boundaries gives the breakdown.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
+        for i in range(chunk):
+            it.step(i % REPLICAS)
+    staged = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(staged, stream=stream):
         for i in range(chunk):
             it.step(i % REPLICAS, evs[i] if evs else None)
     # the same iteration with the capture compiled out of verify (select then
@@ -246,6 +253,7 @@ def run_gpu(args, rank, world, dist):
             it.step(i % REPLICAS, evp[i] if evp else None, capture=False)
     with torch.cuda.stream(stream):
         graph.replay()
+        staged.replay()
         plain.replay()
     stream.synchronize()
 
@@ -266,7 +274,10 @@ def run_gpu(args, rank, world, dist):
     if dist:
         dist.barrier()
     ms_total = t0.elapsed_time(t1)
-    # plain verify (capture compiled out), same rotation, for the capture overhead
+    # the stage breakdown (event nodes between stages), then plain verify
+    # (capture compiled out), same rotation, for the capture overhead
+    with torch.cuda.stream(stream):
+        staged.replay()
     p0 = torch.cuda.Event(enable_timing=True)
     p1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -296,7 +307,8 @@ def run_gpu(args, rank, world, dist):
         d = [evs[i][2].elapsed_time(evs[i][3]) for i in range(chunk)]
         stages = {"verify_us": 1000 * statistics.mean(v), "select_us": 1000 * statistics.mean(s),
                   "draft_us_per_step": 1000 * statistics.mean(d) / w.gamma,
-                  "source": "external CUDA events in the replayed graph (last replay)"}
+                  "source": "external CUDA events at the stage boundaries of a separately "
+                            "replayed graph (events there serialise the stages)"}
     e2e = run_e2e(it, stream, min(K_eff, 500), nbytes)
     return it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e
 

@@ -101,6 +101,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 }
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelectParams p) {
+  griddep_begin();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
@@ -403,13 +404,15 @@ cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStr
   cfg.blockDim = dim3(kSelThreads, 1, 1);
   cfg.dynamicSmemBytes = select_smem_bytes(p.chunk);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, select_topk_kernel, p);
 }
 

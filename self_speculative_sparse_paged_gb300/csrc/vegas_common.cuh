@@ -243,6 +243,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn_major, 
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) |
          (uint32_t(b_mn_major) << 16) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
+// Programmatic dependent launch.  Every hot-path kernel is launched so that it
+// may start while the previous kernel of the stream drains; before touching
+// global memory it waits until that kernel has completed and its writes are
+// visible, and it lets the next kernel start launching right away.  Without
+// the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_begin() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // True in exactly one lane of the (fully active) warp.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;

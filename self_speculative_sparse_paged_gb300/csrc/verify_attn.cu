@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(VerifyCfg<D, NT>::W * 32, 1)
   constexpr int QROW = 2 * D + 16;
   constexpr bool QS = Cfg::kQSmem;
 
+  griddep_begin();
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -316,9 +318,17 @@ static cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(p.num_splits, p.hkv, batch);
-  verify_attn_kernel<D, NT, CAP><<<grid, Cfg::W * 32, Cfg::kSmem, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits, p.hkv, batch);
+  cfg.blockDim = dim3(Cfg::W * 32, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_attn_kernel<D, NT, CAP>, kmap, vmap, p);
 }
 
 template <>

@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(384, 1)
   static_assert(NQP == 16 || NQP == 32, "MMA N");
   static_assert(NQC % 8 == 0 && NQC <= NQP, "processed columns");
 
+  griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -649,13 +650,15 @@ static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.cluster_merge ? p.num_splits : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch ? 2 : 1;
   if (!launch) return cudaOccupancyMaxActiveClusters(clusters, verify_tc_kernel<NQP, NQC, CAP>, &cfg);
   return cudaLaunchKernelEx(&cfg, verify_tc_kernel<NQP, NQC, CAP>, kmap, vmap, p);
 }
