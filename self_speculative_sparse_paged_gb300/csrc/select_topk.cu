@@ -10,8 +10,7 @@
 // -0.0 equal to +0.0, NaN lowest).  One thread-block cluster per (KV head,
 // sequence); each CTA keeps its chunk of keys in shared memory.  The k-th
 // largest key tau is found by narrowing a key interval [klo, khi] that holds
-// it, one 2048-bin histogram per level, summed over the cluster through
-// distributed shared memory:
+// it, one 2048-bin histogram per level:
 //   level 0 counts the values in 2048 equal bins of the unit's [min, max] (a
 //           monotone map, so every bin is a key interval and the bins fill
 //           evenly);
@@ -20,11 +19,18 @@
 //           below the span's top bit.
 // From level 1 on, every bin also records its smallest and largest key, so
 // the chosen bin gives the next [klo, khi] exactly and the search ends as soon
-// as that interval holds one key value (usually after level 1; at most five
-// levels).  Then every
-// key > tau is taken and keys == tau in position order until k are chosen;
-// warp ballots plus the warps' and CTAs' counts place each chosen position at
-// its rank, so the output is ascending and deterministic.
+// as that interval holds one key value (usually after level 1).
+//
+// Each CTA also sums its histogram into 64 super-bins of 32 bins.  After one
+// cluster barrier per level, warp 0 of every CTA reads the 64 super-bin counts
+// of all CTAs through distributed shared memory, then the 32 bins of the
+// chosen super-bin, then the chosen bin's key range: three small remote reads
+// instead of every CTA reading every histogram.  The same reads give, per CTA
+// of the cluster, how many of its keys lie above the chosen bin (and, at the
+// last level, inside it), so each CTA knows how many chosen positions precede
+// its own without another exchange.  Every key > tau is taken and keys == tau
+// in position order until k are chosen; warp ballots place each chosen
+// position at its rank, so the output is ascending and deterministic.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -38,8 +44,17 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelMaxChunk = 32768;                 // keys per CTA
 constexpr int kSelChunkQuantum = 8 * kSelThreads;   // chunks hold 8 keys per thread at a time
-constexpr int kBins = 2048;                         // 4 per thread
-constexpr int kLevelWords = 6 * kBins;              // two sets of {count, min key, max key}
+constexpr int kBins = 2048;
+constexpr int kSuper = 64;                          // super-bins of kFine bins
+constexpr int kFine = kBins / kSuper;               // 32: one per lane
+constexpr int kMaxSelCluster = 8;
+// two sets (one per level parity) of {count, min key, max key} per bin, and
+// super-bin counts
+constexpr int kLevelWords = 6 * kBins + 2 * kSuper;
+
+// Binning of a level: value bins of [min, max] (counts only), sub-bins of the
+// chosen value bin, bits of key - klo; kDone once [klo, khi] holds one key.
+enum { kValueBins, kSubBins, kKeyBits, kDone };
 
 // Larger float -> larger key; -0.0 equals +0.0; NaN below every number.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -54,12 +69,6 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-constexpr int kMaxSelCluster = 8;
-
-// Binning of a level: value bins of [min, max] (counts only), sub-bins of the
-// chosen value bin, bits of key - klo; kDone once [klo, khi] holds one key.
-enum { kValueBins, kSubBins, kKeyBits, kDone };
-
 constexpr uint32_t kKeyNegInf = 0x007fffffu;   // order_key(-inf)
 constexpr uint32_t kKeyPosInf = 0xff800000u;   // order_key(+inf)
 
@@ -70,34 +79,112 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Exclusive scan over the block; returns the exclusive prefix, sets total.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot,
-                                                         uint32_t& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t inc = v;
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += t;
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
   }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t w = lane < kSelWarps ? warp_tot[lane] : 0u;
-    uint32_t wi = w;
+  return v;
+}
+
+// Shared state of the level search, written by warp 0.
+struct SelState {
+  uint32_t bin, above, klo, khi;
+  uint32_t gt[kMaxSelCluster];    // per CTA: keys above the chosen bins so far
+  uint32_t in[kMaxSelCluster];    // per CTA: keys inside this level's chosen bin
+};
+
+// Warp 0: finds the bin holding the need-th largest key from the cluster's
+// histograms of one set (counts `cnt`, super-bin counts `sup`, key bounds
+// `bmn`/`bmx` unless `bounds` is false) and records it in `st`.
+__device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
+                                             const uint32_t* cnt, const uint32_t* sup,
+                                             const uint32_t* bmn, const uint32_t* bmx,
+                                             bool bounds, uint32_t need, SelState& st) {
+  const int lane = threadIdx.x & 31;
+  // super-bins 63 - 2 lane (hi) and 62 - 2 lane (lo): descending with the lane
+  const int sbh = kSuper - 1 - 2 * lane, sbl = sbh - 1;
+  uint32_t ch[kMaxSelCluster], cl[kMaxSelCluster];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += t;
+  for (int q = 0; q < kMaxSelCluster; ++q) {
+    ch[q] = cl[q] = 0u;
+    if (q < CL) {
+      const uint2 x = *reinterpret_cast<const uint2*>(cluster.map_shared_rank(sup + sbl, q));
+      cl[q] = x.x;
+      ch[q] = x.y;
     }
-    warp_tot[lane] = wi - w;
-    if (lane == 31) warp_tot[32] = wi;
   }
-  __syncthreads();
-  const uint32_t ex = warp_tot[warp] + inc - v;
-  total = warp_tot[32];
-  __syncthreads();
-  return ex;
+  uint32_t th = 0, tl = 0;
+#pragma unroll
+  for (int q = 0; q < kMaxSelCluster; ++q) {
+    th += ch[q];
+    tl += cl[q];
+  }
+  const uint32_t incl = warp_inclusive_scan(th + tl), excl = incl - th - tl;
+  const bool hit = excl < need && need <= incl;
+  const int hlane = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+  int sb = 0;
+  uint32_t above = 0;
+  if (hit) {
+    if (need <= excl + th) {
+      sb = sbh;
+      above = excl;
+    } else {
+      sb = sbl;
+      above = excl + th;
+    }
+  }
+  sb = __shfl_sync(0xffffffffu, sb, hlane);
+  above = __shfl_sync(0xffffffffu, above, hlane);
+  // the 32 bins of super-bin sb, bin sb * 32 + 31 - lane (descending with the lane)
+  const int fb = sb * kFine + (kFine - 1 - lane);
+  uint32_t f[kMaxSelCluster];
+#pragma unroll
+  for (int q = 0; q < kMaxSelCluster; ++q) f[q] = q < CL ? cluster.map_shared_rank(cnt, q)[fb] : 0u;
+  uint32_t ft = 0;
+#pragma unroll
+  for (int q = 0; q < kMaxSelCluster; ++q) ft += f[q];
+  const uint32_t fincl = warp_inclusive_scan(ft), fexcl = fincl - ft;
+  const uint32_t need2 = need - above;
+  const bool hit2 = fexcl < need2 && need2 <= fincl;
+  const int hl2 = __ffs(__ballot_sync(0xffffffffu, hit2)) - 1;
+  const int bin = sb * kFine + (kFine - 1 - hl2);
+  const uint32_t above_bin = above + __shfl_sync(0xffffffffu, fexcl, hl2);
+  // per CTA: keys in bins above the chosen one, and inside it
+#pragma unroll
+  for (int q = 0; q < kMaxSelCluster; ++q) {
+    const uint32_t up = (sbh > sb ? ch[q] : 0u) + (sbl > sb ? cl[q] : 0u) + (lane < hl2 ? f[q] : 0u);
+    const uint32_t gtq = warp_sum(up);
+    const uint32_t inq = __shfl_sync(0xffffffffu, f[q], hl2);
+    if (lane == 0 && q < CL) {
+      st.gt[q] += gtq;
+      st.in[q] = inq;
+    }
+  }
+  // key bounds of the chosen bin over the cluster
+  uint32_t a = 0xffffffffu, z = 0u;
+  if (bounds && lane < CL) {
+    a = cluster.map_shared_rank(bmn, lane)[bin];
+    z = cluster.map_shared_rank(bmx, lane)[bin];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+    z = max(z, __shfl_xor_sync(0xffffffffu, z, o));
+  }
+  if (lane == 0) {
+    st.bin = (uint32_t)bin;
+    st.above = above_bin;
+    st.klo = a;
+    st.khi = z;
+  }
 }
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelectParams p) {
@@ -110,14 +197,29 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   const int unit = b * p.hkv + g;
 
   extern __shared__ __align__(16) uint32_t smem[];
-  uint32_t* cnt = smem;                    // [2][kBins] keys per bin (one set per level parity)
+  uint32_t* cnt = smem;                    // [2][kBins] keys per bin
   uint32_t* bmn = smem + 2 * kBins;        // [2][kBins] smallest key of each bin
   uint32_t* bmx = smem + 4 * kBins;        // [2][kBins] largest key of each bin
+  uint32_t* sup = smem + 6 * kBins;        // [2][kSuper] keys per super-bin
   uint32_t* keys = smem + kLevelWords;     // [chunk]
-  __shared__ uint32_t warp_tot[33];
   __shared__ uint32_t red[2 * kSelWarps];
-  __shared__ uint32_t xch[4];              // read by the cluster: key range, then counts
-  __shared__ uint32_t sel[4];              // chosen bin: keys above it, min and max key, index
+  __shared__ uint32_t xch[2];              // read by the cluster: this CTA's key range
+  __shared__ SelState st;
+
+  // Warp w owns chunk offsets r = 32 P w + 32 u + lane, u < P: contiguous per
+  // warp, so position order is (rank, warp, u, lane).  The first keys are
+  // requested before the sequence length is known (within the score row).
+  const int P = p.chunk / kSelThreads;
+  const int start = rank * p.chunk;
+  const int lim = max(0, min(p.chunk, p.score_stride - start));
+  const int r0 = warp * 32 * P + lane;
+  const float* src = p.scores + size_t(unit) * p.score_stride + start;
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0 + i * 32;
+    v[i] = r < lim ? __ldcg(src + r) : 0.f;
+  }
 
   int L = p.ctx_lens[b];
   int k = p.k_per_seq[b];
@@ -133,27 +235,26 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     for (int j = rank * kSelThreads + tid; j < L; j += CL * kSelThreads) out[j] = j;
     return;
   }
-
-  // Warp w owns chunk offsets r = 32 P w + 32 u + lane, u < P: contiguous per
-  // warp, so position order is (rank, warp, u, lane).
-  const int P = p.chunk / kSelThreads;
-  const int start = rank * p.chunk;
   const int nvalid = max(0, min(p.chunk, L - start));
-  const int r0 = warp * 32 * P + lane;
-  const float* src = p.scores + size_t(unit) * p.score_stride + start;
 
   for (int i = tid; i < 2 * kBins; i += kSelThreads) {
     cnt[i] = 0u;
     bmn[i] = 0xffffffffu;
     bmx[i] = 0u;
   }
+  if (tid < 2 * kSuper) sup[tid] = 0u;
+  if (tid < kMaxSelCluster) {
+    st.gt[tid] = 0u;
+    st.in[tid] = 0u;
+  }
   uint32_t kmin = 0xffffffffu, kmax = 0u;
   for (int u0 = 0; u0 < P; u0 += 8) {
-    float v[8];
+    if (u0 > 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = r0 + (u0 + i) * 32;
-      v[i] = r < nvalid ? __ldcg(src + r) : 0.f;
+      for (int i = 0; i < 8; ++i) {
+        const int r = r0 + (u0 + i) * 32;
+        v[i] = r < nvalid ? __ldcg(src + r) : 0.f;
+      }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -217,9 +318,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   const bool linear = kmin > kKeyNegInf && kmax < kKeyPosInf && range > 1.0e-30f && range < 3.0e38f;
   const float scale = linear ? float(kBins) / range : 0.f;
   int mode = klo == khi ? kDone : (linear ? kValueBins : kKeyBits);
+  const bool searched = mode != kDone;
   uint32_t vbin = 0;              // chosen value bin (kSubBins)
   for (int level = 0; mode != kDone; ++level) {
-    const int s = (level & 1) * kBins;
+    const int s = level & 1;
+    uint32_t* c = cnt + s * kBins;
+    uint32_t* mn = bmn + s * kBins;
+    uint32_t* mx = bmx + s * kBins;
+    uint32_t* su = sup + s * kSuper;
     const int lo = mode == kKeyBits ? max(0, (32 - __clz(khi - klo)) - 11) : 0;
     for (int u = 0; u < P; ++u) {
       const int r = r0 + u * 32;
@@ -233,7 +339,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
         const float t = __fmul_rn(__fsub_rn(key_value(key), vmin), scale);
         const uint32_t bin = min((uint32_t)kBins - 1u, __float2uint_rz(fmaxf(0.f, t)));
         if (mode == kValueBins) {       // counts only: every key takes part
-          atomicAdd(&cnt[s + bin], 1u);
+          atomicAdd(&c[bin], 1u);
           continue;
         }
         if (bin != vbin) continue;
@@ -241,79 +347,53 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
         d = min((uint32_t)kBins - 1u,
                 __float2uint_rz(fmaxf(0.f, __fmul_rn(__fsub_rn(t, float(vbin)), float(kBins)))));
       }
-      atomicAdd(&cnt[s + d], 1u);
-      atomicMin(&bmn[s + d], key);
-      atomicMax(&bmx[s + d], key);
-    }
-    cluster.sync();
-    // The other set's last readers (the previous level) are past this barrier.
-    for (int i = tid; i < kBins; i += kSelThreads) {
-      cnt[(kBins - s) + i] = 0u;
-      bmn[(kBins - s) + i] = 0xffffffffu;
-      bmx[(kBins - s) + i] = 0u;
-    }
-    // Thread t owns bins b0 + 3 .. b0 (descending), b0 = kBins - 4 (t + 1).
-    const int b0 = kBins - 4 * (tid + 1);
-    uint4 x[kMaxSelCluster];
-#pragma unroll
-    for (int q = 0; q < kMaxSelCluster; ++q)
-      if (q < CL) x[q] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(cnt + s + b0, q));
-    uint32_t h3 = 0, h2 = 0, h1 = 0, h0 = 0;
-#pragma unroll
-    for (int q = 0; q < kMaxSelCluster; ++q) {
-      if (q < CL) {
-        h3 += x[q].w;
-        h2 += x[q].z;
-        h1 += x[q].y;
-        h0 += x[q].x;
-      }
-    }
-    uint32_t total;
-    uint32_t above = block_exclusive_scan(h3 + h2 + h1 + h0, warp_tot, total);
-    int chosen = -1;
-    if (above < need && need <= above + h3) chosen = b0 + 3;
-    else if ((above += h3) < need && need <= above + h2) chosen = b0 + 2;
-    else if ((above += h2) < need && need <= above + h1) chosen = b0 + 1;
-    else if ((above += h1) < need && need <= above + h0) chosen = b0;
-    if (chosen >= 0) {
-      uint32_t a = 0xffffffffu, c = 0u;
-      if (mode != kValueBins) {
-        uint32_t mn[kMaxSelCluster], mx[kMaxSelCluster];
-#pragma unroll
-        for (int q = 0; q < kMaxSelCluster; ++q) {
-          if (q < CL) {
-            mn[q] = cluster.map_shared_rank(bmn + s, q)[chosen];
-            mx[q] = cluster.map_shared_rank(bmx + s, q)[chosen];
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < kMaxSelCluster; ++q) {
-          if (q < CL) {
-            a = min(a, mn[q]);
-            c = max(c, mx[q]);
-          }
-        }
-      }
-      sel[0] = above;
-      sel[1] = a;
-      sel[2] = c;
-      sel[3] = (uint32_t)chosen;
+      atomicAdd(&c[d], 1u);
+      atomicMin(&mn[d], key);
+      atomicMax(&mx[d], key);
     }
     __syncthreads();
-    need -= sel[0];
+    // super-bin sums: warp w adds super-bins 4w .. 4w + 3
+#pragma unroll
+    for (int j = 0; j < kSuper / kSelWarps; ++j) {
+      const int sb = (kSuper / kSelWarps) * warp + j;
+      const uint32_t x = warp_sum(c[sb * kFine + lane]);
+      if (lane == 0) su[sb] = x;
+    }
+    cluster.sync();
+    // The other set's last readers (the previous level's search) are past
+    // this barrier: clear it for the next level.
+    {
+      const int o = (s ^ 1) * kBins;
+      for (int i = tid; i < kBins; i += kSelThreads) {
+        cnt[o + i] = 0u;
+        bmn[o + i] = 0xffffffffu;
+        bmx[o + i] = 0u;
+      }
+      if (tid < kSuper) sup[(s ^ 1) * kSuper + tid] = 0u;
+    }
+    if (warp == 0) search_level(cluster, CL, c, su, mn, mx, mode != kValueBins, need, st);
+    __syncthreads();
+    need -= st.above;
     if (mode == kValueBins) {
-      vbin = sel[3];
+      vbin = st.bin;
       mode = kSubBins;
     } else {
-      klo = sel[1];
-      khi = sel[2];
+      klo = st.klo;
+      khi = st.khi;
       mode = klo == khi ? kDone : kKeyBits;
     }
-    __syncthreads();   // sel is rewritten by the next level
   }
+  cluster_arrive();   // no shared memory of another CTA is read after this point
   const uint32_t tau = klo;       // `need` keys equal to tau are taken, lowest positions first
 
-  // ---- compaction in position order
+  // chosen keys before this CTA's (gt) and keys equal to tau before it (eq)
+  uint32_t gt = 0, eq = 0;
+  for (int q = 0; q < rank; ++q) {
+    gt += searched ? st.gt[q] : 0u;
+    eq += searched ? st.in[q] : (uint32_t)max(0, min(p.chunk, L - q * p.chunk));
+  }
+
+  // ---- compaction in position order: per-warp counts, then ballot ranks
   uint32_t n_gt = 0, n_eq = 0;
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
@@ -330,46 +410,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   if (warp == 0) {
     const uint32_t a = lane < kSelWarps ? red[lane] : 0u;
     const uint32_t c = lane < kSelWarps ? red[kSelWarps + lane] : 0u;
-    uint32_t ia = a, ic = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t ta = __shfl_up_sync(0xffffffffu, ia, o);
-      const uint32_t tc = __shfl_up_sync(0xffffffffu, ic, o);
-      if (lane >= o) {
-        ia += ta;
-        ic += tc;
-      }
-    }
+    const uint32_t ia = warp_inclusive_scan(a), ic = warp_inclusive_scan(c);
+    __syncwarp();
     if (lane < kSelWarps) {
       red[lane] = ia - a;
       red[kSelWarps + lane] = ic - c;
     }
-    if (lane == 31) {
-      xch[2] = ia;
-      xch[3] = ic;
-    }
   }
-  cluster.sync();
-  uint32_t gt = red[warp], eq = red[kSelWarps + warp];   // selected keys before this warp's
-  {
-    uint32_t a[kMaxSelCluster - 1], c[kMaxSelCluster - 1];
-#pragma unroll
-    for (int q = 0; q < kMaxSelCluster - 1; ++q) {
-      if (q < rank) {
-        const uint32_t* x = cluster.map_shared_rank(xch, q);
-        a[q] = x[2];
-        c[q] = x[3];
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kMaxSelCluster - 1; ++q) {
-      if (q < rank) {
-        gt += a[q];
-        eq += c[q];
-      }
-    }
-  }
-  cluster_arrive();   // this CTA reads no other CTA's shared memory after here
+  __syncthreads();
+  gt += red[warp];
+  eq += red[kSelWarps + warp];
   const uint32_t below = (1u << lane) - 1u;
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
