@@ -54,6 +54,48 @@ def read_peaks():
         return 6800.0, "fallback"
 
 
+# DRAM traffic of one verify launch (dram__bytes_read.sum + dram__bytes_write.sum)
+# on this workload, from the ncu launch list in
+# profiles/launch_list_qwen3_8b_b1_32k.md; reported only while the kernel
+# sources still hash to the digest they had when the counters were taken.
+VERIFY_TRAFFIC = {
+    "bytes": 137_520_000,
+    "sources": ["verify_tc.cu", "split_merge.cuh", "attn_core.cuh", "vegas_common.cuh",
+                "kernels.h"],
+    "sha256": "3c32cf41dc99e9e052465fc36232fbeb428dbf477e6898bc1184167bff881234",
+}
+
+
+def verify_traffic_bytes():
+    import hashlib
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "self_speculative_sparse_paged_gb300", "csrc")
+    h = hashlib.sha256()
+    try:
+        for f in VERIFY_TRAFFIC["sources"]:
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return VERIFY_TRAFFIC["bytes"] if h.hexdigest() == VERIFY_TRAFFIC["sha256"] else None
+
+
+def max_over_ranks(value, dist, device=None):
+    """The largest value over the ranks (the slowest rank's time); value itself
+    when there is no process group."""
+    if not dist:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_step, ms_per_step, world):
+    """Whole-job throughput: every rank moves bytes_per_step per step (replicas)."""
+    return bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def algorithmic_bytes(w, lens, kps):
     """Bytes one iteration must move, by stage."""
     d, hkv, hq, T = w.head_dim, w.hkv, w.hq, w.gamma + 1
@@ -294,10 +336,7 @@ def run_gpu(args, rank, world, dist):
     else:
         verify_plain_us = float("nan")
 
-    if dist:
-        tm = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms_total = float(tm.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K_eff
 
     stages = None
@@ -437,12 +476,13 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        ref = time_oracle(w, nbytes, budget_s=150.0, min_steps=args.steps + args.warmup,
-                          max_steps=args.steps + args.warmup)
+        # At most --steps oracle unit steps (one KV head of the iteration each),
+        # stopped once 150 s of them have run, so the arm ends within minutes.
+        ref = time_oracle(w, nbytes, budget_s=150.0, min_steps=1, max_steps=args.steps)
         gbs = ref["value"]
         us = nbytes["total"] / (gbs * 1e9) * 1e6
         line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
-                "n_gpus": args.gpus, "steps": ref["steps"], "warmup": 0,
+                "n_gpus": args.gpus, "steps": ref["steps"], "warmup": 1,
                 "ms_per_step": round(us / 1000, 3), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": base_config(w, lens, kps),
@@ -461,8 +501,9 @@ def main():
     it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e = run_gpu(args, rank, world,
                                                                               dist)
     us_step = ms_step * 1000.0
-    gbs = nbytes["total"] / (us_step * 1e-6) / 1e9
-    line = {"metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s",
+    gbs = job_gbs(nbytes["total"], ms_step, 1)
+    line = {"metric": METRIC, "value": round(job_gbs(nbytes["total"], ms_step, world), 2),
+            "unit": "GB/s",
             "n_gpus": world, "steps": K_eff, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 5), "us_per_iteration": round(us_step, 2),
             "pct_of_8tbs": round(100 * gbs / (ROOFLINE_TBS * 1000), 2),
@@ -481,7 +522,7 @@ def main():
         line["roofline"] = {"kernel": "verify_attn_kernel", "bound": "hbm",
                             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                            "traffic": None,
+                            "traffic": verify_traffic_bytes(),
                             "bytes_per_launch": nbytes["verify"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ref = time_oracle(it.w, nbytes, budget_s=15.0)

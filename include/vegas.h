@@ -30,8 +30,14 @@
  *    matching *_workspace_size() reports, zero-filled once before their first
  *    use (e.g. cudaMemsetAsync).  Every call leaves the workspace's counters
  *    at zero again.  A workspace must not be shared by calls that may run
- *    concurrently.
+ *    concurrently.  A reported size of 0 means the call needs none (NULL is
+ *    accepted).
  *  - The library allocates no device memory in these calls.
+ *  - Kernels are launched with programmatic dependent launch: each may begin
+ *    while the previous kernel of the stream drains, and waits for that
+ *    kernel to complete (griddepcontrol.wait) before touching global memory.
+ *    A caller kernel launched with the same attribute right after one of
+ *    these calls must wait likewise before reading its outputs.
  */
 #ifndef VEGAS_H_
 #define VEGAS_H_

@@ -7,10 +7,13 @@
 // "Collect-2-Query", §3 "Implementation"), used when the unit's query columns
 // (the (gamma+1)*G rows plus the two capture columns) fit in 32.
 //
-// One CTA per (split, KV head, sequence), 10 warps:
-//   warp 0     TMA producer: lanes 0..7 each load one page of K and of V of a
-//              128-position tile (8 pages) into a 3-deep ring of stages;
-//   warp 1     allocates tensor memory; lane 0 issues the MMAs
+// One CTA per (split, KV head, sequence), 12 warps:
+//   warps 0, 10, 11  TMA producers (issue rate is per warp, so a tile's 32
+//              boxes are spread over three warps): K and V tiles of 128
+//              positions (8 pages) stream into 3-slot K and V rings, block-table
+//              entries prefetched four tiles ahead;
+//   warp 1     allocates tensor memory; the warp runs the MMA loop uniformly
+//              and one elected lane issues
 //                S^T[128 pos x N] = K[128 x 128] . Q^T   (both K-major, the K
 //                tile consumed straight from the TMA's 128-byte swizzle),
 //                O^T[128 d x N]  += V^T[128 x 128] . P^T (V read MN-major);
@@ -25,6 +28,10 @@
 // 8 (one vote per group); only then is the group's O^T rescaled in tensor
 // memory.  It writes P^T = 2^(x - m) as bf16 into a 128-byte-swizzled shared
 // buffer that the PV MMA reads.
+//
+// Splits of a unit merge either on chip, when all of them form one
+// thread-block cluster (distributed shared memory, no workspace), or through
+// the workspace in the last-arriving CTA.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
