@@ -61,7 +61,7 @@ struct SelectParams {
   int score_stride;
   int hkv;
   int k_max;
-  int chunk;                // keys per CTA of a cluster, a multiple of select_chunk_quantum()
+  int chunk;                // keys per CTA of a cluster: 1, 2, 4 or 8 x select_chunk_quantum()
   int* err;
 };
 

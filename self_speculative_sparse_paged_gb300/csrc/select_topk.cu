@@ -21,11 +21,13 @@
 // the chosen bin gives the next [klo, khi] exactly and the search ends as soon
 // as that interval holds one key value (usually after level 1).
 //
-// Each CTA also sums its histogram into 64 super-bins of 32 bins.  After one
-// cluster barrier per level, warp 0 of every CTA reads the 64 super-bin counts
-// of all CTAs through distributed shared memory, then the 32 bins of the
-// chosen super-bin, then the chosen bin's key range: three small remote reads
-// instead of every CTA reading every histogram.  The same reads give, per CTA
+// Each CTA also sums its histogram into 64 super-bins of 32 bins and pushes
+// them (and, once, its key range) into every CTA of the cluster with remote
+// stores.  After one cluster barrier per level, warp 0 of every CTA scans the
+// super-bin counts locally and reads the counts and key bounds of the 32 bins
+// of the chosen super-bin from every CTA through distributed shared memory:
+// one small remote read per level instead of every CTA reading every
+// histogram.  The same reads give, per CTA
 // of the cluster, how many of its keys lie above the chosen bin (and, at the
 // last level, inside it), so each CTA knows how many chosen positions precede
 // its own without another exchange.  Every key > tau is taken and keys == tau
@@ -43,14 +45,14 @@ namespace vegas {
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelMaxChunk = 32768;                 // keys per CTA
-constexpr int kSelChunkQuantum = 8 * kSelThreads;   // chunks hold 8 keys per thread at a time
+constexpr int kSelChunkQuantum = 8 * kSelThreads;   // chunks are 1, 2, 4 or 8 quanta (8-64 keys a thread)
 constexpr int kBins = 2048;
 constexpr int kSuper = 64;                          // super-bins of kFine bins
 constexpr int kFine = kBins / kSuper;               // 32: one per lane
 constexpr int kMaxSelCluster = 8;
-// two sets (one per level parity) of {count, min key, max key} per bin, and
-// super-bin counts
-constexpr int kLevelWords = 6 * kBins + 2 * kSuper;
+// two sets (one per level parity) of {count, min key, max key} per bin, and of
+// every CTA's super-bin counts
+constexpr int kLevelWords = 6 * kBins + 2 * kMaxSelCluster * kSuper;
 
 // Binning of a level: value bins of [min, max] (counts only), sub-bins of the
 // chosen value bin, bits of key - klo; kDone once [klo, khi] holds one key.
@@ -102,21 +104,23 @@ struct SelState {
 };
 
 // Warp 0: finds the bin holding the need-th largest key from the cluster's
-// histograms of one set (counts `cnt`, super-bin counts `sup`, key bounds
-// `bmn`/`bmx` unless `bounds` is false) and records it in `st`.
+// histograms of one set (counts `cnt` and key bounds `bmn`/`bmx`, unless
+// `bounds` is false, read remotely; super-bin counts of every CTA in the local
+// `sup_all`) and records it in `st`.
 __device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
-                                             const uint32_t* cnt, const uint32_t* sup,
+                                             const uint32_t* cnt, const uint32_t* sup_all,
                                              const uint32_t* bmn, const uint32_t* bmx,
                                              bool bounds, uint32_t need, SelState& st) {
   const int lane = threadIdx.x & 31;
-  // super-bins 63 - 2 lane (hi) and 62 - 2 lane (lo): descending with the lane
+  // super-bins 63 - 2 lane (hi) and 62 - 2 lane (lo): descending with the lane;
+  // every CTA's counts were pushed into this CTA's sup_all[q][kSuper]
   const int sbh = kSuper - 1 - 2 * lane, sbl = sbh - 1;
   uint32_t ch[kMaxSelCluster], cl[kMaxSelCluster];
 #pragma unroll
   for (int q = 0; q < kMaxSelCluster; ++q) {
     ch[q] = cl[q] = 0u;
     if (q < CL) {
-      const uint2 x = *reinterpret_cast<const uint2*>(cluster.map_shared_rank(sup + sbl, q));
+      const uint2 x = *reinterpret_cast<const uint2*>(sup_all + q * kSuper + sbl);
       cl[q] = x.x;
       ch[q] = x.y;
     }
@@ -145,9 +149,21 @@ __device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
   above = __shfl_sync(0xffffffffu, above, hlane);
   // the 32 bins of super-bin sb, bin sb * 32 + 31 - lane (descending with the lane)
   const int fb = sb * kFine + (kFine - 1 - lane);
-  uint32_t f[kMaxSelCluster];
+  // counts and key bounds of the lane's bin in every CTA, in one round trip
+  uint32_t f[kMaxSelCluster], fmn[kMaxSelCluster], fmx[kMaxSelCluster];
 #pragma unroll
-  for (int q = 0; q < kMaxSelCluster; ++q) f[q] = q < CL ? cluster.map_shared_rank(cnt, q)[fb] : 0u;
+  for (int q = 0; q < kMaxSelCluster; ++q) {
+    f[q] = 0u;
+    fmn[q] = 0xffffffffu;
+    fmx[q] = 0u;
+    if (q < CL) {
+      f[q] = cluster.map_shared_rank(cnt, q)[fb];
+      if (bounds) {
+        fmn[q] = cluster.map_shared_rank(bmn, q)[fb];
+        fmx[q] = cluster.map_shared_rank(bmx, q)[fb];
+      }
+    }
+  }
   uint32_t ft = 0;
 #pragma unroll
   for (int q = 0; q < kMaxSelCluster; ++q) ft += f[q];
@@ -168,17 +184,15 @@ __device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
       st.in[q] = inq;
     }
   }
-  // key bounds of the chosen bin over the cluster
+  // key bounds of the chosen bin over the cluster (held by lane hl2)
   uint32_t a = 0xffffffffu, z = 0u;
-  if (bounds && lane < CL) {
-    a = cluster.map_shared_rank(bmn, lane)[bin];
-    z = cluster.map_shared_rank(bmx, lane)[bin];
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
-    z = max(z, __shfl_xor_sync(0xffffffffu, z, o));
+  for (int q = 0; q < kMaxSelCluster; ++q) {
+    a = min(a, fmn[q]);
+    z = max(z, fmx[q]);
   }
+  a = __shfl_sync(0xffffffffu, a, hl2);
+  z = __shfl_sync(0xffffffffu, z, hl2);
   if (lane == 0) {
     st.bin = (uint32_t)bin;
     st.above = above_bin;
@@ -187,6 +201,8 @@ __device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
   }
 }
 
+// P keys per thread (the CTA's chunk is kSelThreads * P keys).
+template <int P>
 __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelectParams p) {
   griddep_begin();
   cg::cluster_group cluster = cg::this_cluster();
@@ -200,16 +216,15 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   uint32_t* cnt = smem;                    // [2][kBins] keys per bin
   uint32_t* bmn = smem + 2 * kBins;        // [2][kBins] smallest key of each bin
   uint32_t* bmx = smem + 4 * kBins;        // [2][kBins] largest key of each bin
-  uint32_t* sup = smem + 6 * kBins;        // [2][kSuper] keys per super-bin
+  uint32_t* sup = smem + 6 * kBins;        // [2][kMaxSelCluster][kSuper] every CTA's super-bin counts
   uint32_t* keys = smem + kLevelWords;     // [chunk]
   __shared__ uint32_t red[2 * kSelWarps];
-  __shared__ uint32_t xch[2];              // read by the cluster: this CTA's key range
+  __shared__ uint32_t xch[2 * kMaxSelCluster];   // every CTA's key range, pushed here
   __shared__ SelState st;
 
   // Warp w owns chunk offsets r = 32 P w + 32 u + lane, u < P: contiguous per
   // warp, so position order is (rank, warp, u, lane).  The first keys are
   // requested before the sequence length is known (within the score row).
-  const int P = p.chunk / kSelThreads;
   const int start = rank * p.chunk;
   const int lim = max(0, min(p.chunk, p.score_stride - start));
   const int r0 = warp * 32 * P + lane;
@@ -242,12 +257,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     bmn[i] = 0xffffffffu;
     bmx[i] = 0u;
   }
-  if (tid < 2 * kSuper) sup[tid] = 0u;
   if (tid < kMaxSelCluster) {
     st.gt[tid] = 0u;
     st.in[tid] = 0u;
   }
   uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
   for (int u0 = 0; u0 < P; u0 += 8) {
     if (u0 > 0) {
 #pragma unroll
@@ -277,35 +292,27 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     red[kSelWarps + warp] = kmax;
   }
   __syncthreads();
-  if (tid == 0) {
-    uint32_t a = 0xffffffffu, c = 0u;
-    for (int w = 0; w < kSelWarps; ++w) {
-      a = min(a, red[w]);
-      c = max(c, red[kSelWarps + w]);
+  if (warp == 0) {
+    // this CTA's key range, pushed into every CTA of the cluster (lane q -> CTA q)
+    uint32_t a = lane < kSelWarps ? red[lane] : 0xffffffffu;
+    uint32_t c = lane < kSelWarps ? red[kSelWarps + lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+      c = max(c, __shfl_xor_sync(0xffffffffu, c, o));
     }
-    xch[0] = a;
-    xch[1] = c;
+    if (lane < CL) {
+      uint32_t* x = cluster.map_shared_rank(xch, lane);
+      x[2 * rank] = a;
+      x[2 * rank + 1] = c;
+    }
   }
   cluster.sync();
-  {
-    uint32_t a[kMaxSelCluster], c[kMaxSelCluster];
-#pragma unroll
-    for (int q = 0; q < kMaxSelCluster; ++q) {
-      if (q < CL) {
-        const uint32_t* x = cluster.map_shared_rank(xch, q);
-        a[q] = x[0];
-        c[q] = x[1];
-      }
-    }
-    kmin = 0xffffffffu;
-    kmax = 0u;
-#pragma unroll
-    for (int q = 0; q < kMaxSelCluster; ++q) {
-      if (q < CL) {
-        kmin = min(kmin, a[q]);
-        kmax = max(kmax, c[q]);
-      }
-    }
+  kmin = 0xffffffffu;
+  kmax = 0u;
+  for (int q = 0; q < CL; ++q) {
+    kmin = min(kmin, xch[2 * q]);
+    kmax = max(kmax, xch[2 * q + 1]);
   }
 
   // ---- narrow [klo, khi] around the k-th largest key
@@ -325,11 +332,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     uint32_t* c = cnt + s * kBins;
     uint32_t* mn = bmn + s * kBins;
     uint32_t* mx = bmx + s * kBins;
-    uint32_t* su = sup + s * kSuper;
+    uint32_t* su = sup + s * kMaxSelCluster * kSuper;
     const int lo = mode == kKeyBits ? max(0, (32 - __clz(khi - klo)) - 11) : 0;
+#pragma unroll
     for (int u = 0; u < P; ++u) {
       const int r = r0 + u * 32;
-      if (r >= nvalid) break;
+      if (r >= nvalid) continue;
       const uint32_t key = keys[r];
       uint32_t d;
       if (mode == kKeyBits) {
@@ -352,12 +360,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
       atomicMax(&mx[d], key);
     }
     __syncthreads();
-    // super-bin sums: warp w adds super-bins 4w .. 4w + 3
+    // super-bin sums: warp w adds super-bins 4w .. 4w + 3 and pushes each
+    // into every CTA's su[rank][.] (lane q -> CTA q)
 #pragma unroll
     for (int j = 0; j < kSuper / kSelWarps; ++j) {
       const int sb = (kSuper / kSelWarps) * warp + j;
       const uint32_t x = warp_sum(c[sb * kFine + lane]);
-      if (lane == 0) su[sb] = x;
+      if (lane < CL) cluster.map_shared_rank(su, lane)[rank * kSuper + sb] = x;
     }
     cluster.sync();
     // The other set's last readers (the previous level's search) are past
@@ -369,7 +378,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
         bmn[o + i] = 0xffffffffu;
         bmx[o + i] = 0u;
       }
-      if (tid < kSuper) sup[(s ^ 1) * kSuper + tid] = 0u;
     }
     if (warp == 0) search_level(cluster, CL, c, su, mn, mx, mode != kValueBins, need, st);
     __syncthreads();
@@ -395,6 +403,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
 
   // ---- compaction in position order: per-warp counts, then ballot ranks
   uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
     const bool valid = r < nvalid;
@@ -421,6 +430,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   gt += red[warp];
   eq += red[kSelWarps + warp];
   const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
     const bool valid = r < nvalid;
@@ -440,12 +450,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
 
 size_t select_smem_bytes(int chunk) { return size_t(kLevelWords + chunk) * 4; }
 
-cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream) {
+template <int P>
+static cudaError_t launch_select_p(const SelectParams& p, int cluster, int batch,
+                                   cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
+    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel<P>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)select_smem_bytes(kSelMaxChunk));
+                                         (int)select_smem_bytes(P * kSelThreads));
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -463,7 +475,17 @@ cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStr
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, select_topk_kernel, p);
+  return cudaLaunchKernelEx(&cfg, select_topk_kernel<P>, p);
+}
+
+cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream) {
+  switch (p.chunk / kSelThreads) {
+    case 8: return launch_select_p<8>(p, cluster, batch, stream);
+    case 16: return launch_select_p<16>(p, cluster, batch, stream);
+    case 32: return launch_select_p<32>(p, cluster, batch, stream);
+    case 64: return launch_select_p<64>(p, cluster, batch, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int select_max_chunk() { return kSelMaxChunk; }

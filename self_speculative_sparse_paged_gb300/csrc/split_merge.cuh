@@ -20,20 +20,22 @@ struct SplitWorkspace {
   float* part_o;    // [units][S][nq][D]
 };
 
-// After every thread of the CTA has written this split's partial (m, l, O):
-// takes the unit's ticket and, in the CTA that arrives last, merges the
-// num_splits partials into bf16 output rows.  Called by all NTH threads of the
-// CTA; `area` is free shared memory of at least 3 * num_splits * nq floats,
-// `flag` one int of shared memory.
+// After every thread of the CTA has written this CTA's partial states (m, l,
+// O): takes the unit's ticket and, in the last of the unit's num_ctas CTAs to
+// arrive, merges the unit's num_splits partials (one or more per CTA) into
+// bf16 output rows.  Called by all NTH threads of the CTA; `area` is free
+// shared memory of at least 3 * num_splits * nq floats, `flag` one int of
+// shared memory.
 template <int D, int NTH, int NQMAX, class OutRow>
-__device__ __forceinline__ void finish_splits(const SplitWorkspace& ws, int unit, int num_splits,
-                                              int nq, OutRow out_row, float* area, int* flag) {
+__device__ __forceinline__ void finish_splits(const SplitWorkspace& ws, int unit, int num_ctas,
+                                              int num_splits, int nq, OutRow out_row,
+                                              float* area, int* flag) {
   constexpr int E = (NQMAX * D + NTH - 1) / NTH;   // elements per thread, nq <= NQMAX
   const int tid = threadIdx.x;
   const int nel = nq * D;
   __threadfence();
   __syncthreads();
-  if (tid == 0) *flag = (atomicAdd(&ws.tickets[unit], 1) == num_splits - 1);
+  if (tid == 0) *flag = (atomicAdd(&ws.tickets[unit], 1) == num_ctas - 1);
   __syncthreads();
   if (!*flag) return;
   __threadfence();
@@ -283,7 +285,7 @@ __device__ __forceinline__ void merge_and_write(const WarpState<D, NT>& st, uint
       }
     }
   }
-  finish_splits<D, NTH, NPAD>(ws, unit, num_splits, nq, out_row, cO, flag);
+  finish_splits<D, NTH, NPAD>(ws, unit, num_splits, num_splits, nq, out_row, cO, flag);
 }
 
 }  // namespace vegas

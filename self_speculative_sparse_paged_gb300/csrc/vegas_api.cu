@@ -189,10 +189,12 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
   const int quantum = pl.tc ? vegas::kTcPagesPerTile : 2;
   pl.pages_per_split = (pl.pages_per_split + quantum - 1) / quantum * quantum;
   pl.splits = (kv->max_pages_per_seq + pl.pages_per_split - 1) / pl.pages_per_split;
+  // the tcgen05 kernel leaves one partial per softmax group (two per split)
+  const size_t parts = size_t(pl.splits) * (pl.tc ? 2 : 1);
   pl.tickets_off = 0;
   pl.ml_off = align256(size_t(units) * 4);
-  pl.o_off = pl.ml_off + align256(size_t(units) * pl.splits * pl.nq * 2 * 4);
-  pl.bytes = pl.o_off + size_t(units) * pl.splits * pl.nq * kv->head_dim * 4;
+  pl.o_off = pl.ml_off + align256(size_t(units) * parts * pl.nq * 2 * 4);
+  pl.bytes = pl.o_off + size_t(units) * parts * pl.nq * kv->head_dim * 4;
   return pl;
 }
 
@@ -344,9 +346,11 @@ VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride
   if (st != VEGAS_OK) return st;
   const int units = batch * num_kv_heads;
   const int quantum = vegas::select_chunk_quantum();
-  auto chunk_for = [&](int c) {
+  auto chunk_for = [&](int c) {   // a power-of-two number of quanta
     const int ch = (score_stride + c - 1) / c;
-    return (ch + quantum - 1) / quantum * quantum;
+    int q = quantum;
+    while (q < ch) q *= 2;
+    return q;
   };
   int cl = 1;
   while (chunk_for(cl) > max_chunk) cl *= 2;

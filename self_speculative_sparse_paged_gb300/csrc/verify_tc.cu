@@ -60,37 +60,44 @@ struct TcCfg {
   static constexpr int kOffBar = kOffP + 2 * kP;
   static constexpr int kNumBars = 2 * KS + 2 * VS + 4 * 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  // misc: tmem slot, flag, votes[2][4], colmax[2][4][NQC], colsum[2][4][NQC],
-  // gm[2][NQC], gl[2][NQC], tlim[NQP]
-  static constexpr size_t kMisc = 16 + 32 + 4 * (16 * NQC + 4 * NQC + NQP);
+  // misc: tmem slot, flag, votes[2][4], colmax[2][4][NQC], colsum[2][4][NQC], tlim[NQP]
+  static constexpr size_t kMisc = 16 + 32 + 4 * (16 * NQC + NQP);
   static constexpr size_t kSmem = size_t(kOffMisc) + kMisc + 1024;
 };
 
+// Floats of one staged partial state: O[n][d] (unnormalised, NQC x 128), then
+// M[NQC] (running maxima, log2 units) and L[NQC] (row sums).
+template <int NQC>
+constexpr int kTcStateFloats = NQC * 128 + 2 * NQC;
+
 // Split-KV merge on chip, when the num_splits CTAs of a (sequence, KV head)
-// unit form one thread-block cluster (rank = split).  Each CTA has staged its
-// state in shared memory at `st`: O[n][d] (unnormalised, NQC x 128), then
-// M[NQC] (running maxima, log2 units) and L[NQC] (row sums).  After a cluster
-// barrier, CTA r merges rows n = r, r + S, ... reading the S states through
+// unit form one thread-block cluster (rank = split; a single split is a
+// cluster of one).  Each CTA has staged the states of its two softmax groups
+// in shared memory at `st` (kTcStateFloats apart).  After a cluster barrier,
+// CTA r merges rows n = r, r + S, ... over the 2 S states read through
 // distributed shared memory (merge rule as in split_merge.cuh), writes bf16
 // rows, and leaves only once no CTA reads its shared memory any more.  Called
 // by every thread of every CTA of the cluster.
 template <int NQC, class OutRow>
 __device__ __forceinline__ void cluster_merge_rows(const float* st, int S, int nq, OutRow out_row) {
   constexpr int D = 128;
+  constexpr int SF = kTcStateFloats<NQC>;
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int r = (int)cluster.block_rank(), tid = threadIdx.x;
+  const int nstates = 2 * S;
   if (tid < 2 * D) {
     const int d = tid & (D - 1);
     for (int n = r + (tid >> 7) * S; n < nq; n += 2 * S) {
-      // eight splits' loads in flight at a time, merged into a running state
+      // eight states' loads in flight at a time, merged into a running state
       float M = kEmptyMax, Lsum = 0.f, O = 0.f;
-      for (int s0 = 0; s0 < S; s0 += 8) {
+      for (int s0 = 0; s0 < nstates; s0 += 8) {
         float ms[8], ls[8], os[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (s0 + j < S) {
-            const float* rs = cluster.map_shared_rank(st, s0 + j);
+          const int sidx = s0 + j;
+          if (sidx < nstates) {
+            const float* rs = cluster.map_shared_rank(st, sidx >> 1) + (sidx & 1) * SF;
             os[j] = rs[n * D + d];
             ms[j] = rs[NQC * D + n];
             ls[j] = rs[NQC * D + NQC + n];
@@ -157,9 +164,7 @@ __global__ void __launch_bounds__(384, 1)
   int* votes = reinterpret_cast<int*>(misc + 16);                // [2][4]
   float* colmax = reinterpret_cast<float*>(misc + 48);           // [2][4][NQC]
   float* colsum = colmax + 8 * NQC;                              // [2][4][NQC]
-  float* gm = colsum + 8 * NQC;                                  // [2][NQC]
-  float* gl = gm + 2 * NQC;                                      // [2][NQC]
-  int* tlim = reinterpret_cast<int*>(gl + 2 * NQC);              // [NQP]
+  int* tlim = reinterpret_cast<int*>(colsum + 8 * NQC);          // [NQP]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -526,7 +531,9 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     if (!ok && i == 0) set_error(p.err, kErrDeviceTimeout);
 
-    // Row sums over the group's 128 positions, then the two groups merge.
+    // Each group's (m, l, O^T) is a partial state of its own, merged together
+    // with the splits' states, so no group waits on the other's arithmetic.
+    // Row sums over the group's 128 positions:
 #pragma unroll
     for (int n = 0; n < NQC; ++n) {
       float v = ls[n];
@@ -534,71 +541,50 @@ __global__ void __launch_bounds__(384, 1)
       for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
       if (lane == 0) colsum[(grp * 4 + q4) * NQC + n] = v;
     }
-    named_bar(1 + grp, 128);
-    if (i < NQC) {
-      const float* cs = colsum + grp * 4 * NQC;
-      gm[grp * NQC + i] = m[i];
-      gl[grp * NQC + i] = (mytiles > 0) ? cs[i] + cs[NQC + i] + cs[2 * NQC + i] + cs[3 * NQC + i]
-                                        : 0.f;
-    }
-    named_bar(3, 256);
-    if (grp == 0) {
-      float o0[NQC], o1[NQC];
+    // this thread's O^T row (head dimension i), unnormalised
+    float o[NQC];
 #pragma unroll
-      for (int n = 0; n < NQC; ++n) o0[n] = o1[n] = 0.f;
-      const bool has0 = ntiles > 0, has1 = ntiles > 1;
-      float v0[NQC / 8][8], v1[NQC / 8][8];
+    for (int n = 0; n < NQC; ++n) o[n] = 0.f;
+    if (mytiles > 0) {
 #pragma unroll
       for (int c = 0; c < NQC / 8; ++c) {
-        if (has0) tmem_ld8(tl + 64 + 8 * c, v0[c]);
-        if (has1) tmem_ld8(tl + 96 + 8 * c, v1[c]);
+        float v8[8];
+        tmem_ld8(tl + o_col + 8 * c, v8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[8 * c + e] = v8[e];
       }
       tmem_ld_wait();
+    }
+    named_bar(1 + grp, 128);
+    float Mg = kEmptyMax, Lg = 0.f;                // column i's state (i < NQC)
+    if (i < NQC) {
+      const float* cs = colsum + grp * 4 * NQC;
+      if (mytiles > 0) Lg = cs[i] + cs[NQC + i] + cs[2 * NQC + i] + cs[3 * NQC + i];
 #pragma unroll
-      for (int c = 0; c < NQC / 8; ++c)
+      for (int n = 0; n < NQC; ++n)
+        if (n == i) Mg = m[n];
+    }
+    // Both groups past their last PV: every MMA has completed and every loaded
+    // tile was consumed, so the K ring is free for the staged states.
+    named_bar(3, 256);
+    if (p.cluster_merge || p.num_splits == 1) {
+      float* st = reinterpret_cast<float*>(smem) + grp * kTcStateFloats<NQC>;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (has0) o0[8 * c + e] = v0[c][e];
-          if (has1) o1[8 * c + e] = v1[c][e];
-        }
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-      const size_t part = size_t(unit) * p.num_splits + split;
-      // All shared-memory reads and the merge arithmetic first, the stores
-      // after: interleaved, every store would order the next column's loads.
-      float Mv[NQC], Lv[NQC];
-#pragma unroll
-      for (int n = 0; n < NQC; ++n) {
-        const float m0 = gm[n], m1 = gm[NQC + n];
-        const float M = fmaxf(m0, m1);
-        const float f0 = has0 ? ex2(m0 - M) : 0.f, f1 = has1 ? ex2(m1 - M) : 0.f;
-        Mv[n] = M;
-        Lv[n] = f0 * gl[n] + f1 * gl[NQC + n];
-        o0[n] = f0 * o0[n] + f1 * o1[n];
+      for (int n = 0; n < NQC; ++n)
+        if (n < p.nq) st[n * D + i] = o[n];
+      if (i < p.nq) {
+        st[NQC * D + i] = Mg;
+        st[NQC * D + NQC + i] = Lg;
       }
+    } else {
+      // partial 2 * split + grp of the unit's 2 * num_splits
+      const size_t part = (size_t(unit) * p.num_splits + split) * 2 + grp;
 #pragma unroll
-      for (int n = 0; n < NQC; ++n) {
-        if (n < p.nq) {
-          const float M = Mv[n], Ls = Lv[n], O = o0[n];
-          if (p.num_splits == 1) {
-            const int t = n / p.group, hl = n - t * p.group;
-            out[((size_t(b) * T + t) * p.hq + g * p.group + hl) * D + i] =
-                __float2bfloat16_rn(Ls > 0.f ? O / Ls : 0.f);
-          } else if (p.cluster_merge) {
-            // this split's state for the cluster merge; the Q and P buffers are free now
-            float* stO = reinterpret_cast<float*>(smem + Cfg::kOffQ);
-            stO[n * D + i] = O;
-            if (i == n) {
-              stO[NQC * D + n] = M;
-              stO[NQC * D + NQC + n] = Ls;
-            }
-          } else {
-            p.part_o[(part * p.nq + n) * D + i] = O;
-            if (i == n) {
-              p.part_ml[(part * p.nq + n) * 2 + 0] = M;
-              p.part_ml[(part * p.nq + n) * 2 + 1] = Ls;
-            }
-          }
-        }
+      for (int n = 0; n < NQC; ++n)
+        if (n < p.nq) p.part_o[(part * p.nq + n) * D + i] = o[n];
+      if (i < p.nq) {
+        p.part_ml[(part * p.nq + i) * 2 + 0] = Mg;
+        p.part_ml[(part * p.nq + i) * 2 + 1] = Lg;
       }
     }
   }
@@ -609,18 +595,18 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
-  if (p.num_splits > 1) {
+  {
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     auto out_row = [&](int n) {
       const int t = n / p.group, hl = n - t * p.group;
       return out + ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D;
     };
-    if (p.cluster_merge) {
-      cluster_merge_rows<NQC>(reinterpret_cast<const float*>(smem + Cfg::kOffQ), p.num_splits,
-                              p.nq, out_row);
+    if (p.cluster_merge || p.num_splits == 1) {
+      // (one split: a cluster of one CTA merging its two group states)
+      cluster_merge_rows<NQC>(reinterpret_cast<const float*>(smem), p.num_splits, p.nq, out_row);
     } else {
       SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
-      finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, p.nq, out_row,
+      finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, 2 * p.num_splits, p.nq, out_row,
                                            reinterpret_cast<float*>(smem), flag);
     }
   }

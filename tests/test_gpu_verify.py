@@ -32,6 +32,7 @@ SMALL = {
     "long_split": C2.with_(ctx_lo=20000, ctx_hi=20000, hkv=2, hq=8),       # 16-CTA clusters
     "cluster3_ragged": C2.with_(ctx_lo=400, ctx_hi=400),                   # 3 splits of 9, 9, 8 pages
     "qwen_b2_mixed": C3.with_(batch=2, ctx_lo=150, ctx_hi=6000),           # one short, one long
+    "tc_ticket_b13": C3.with_(batch=13, ctx_lo=600, ctx_hi=900),           # 104 units: workspace merge
 }
 
 
