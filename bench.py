@@ -205,6 +205,7 @@ class GpuIteration:
         self.out_d = torch.empty_like(self.qd)
         self.scores = torch.empty((w.batch, w.hkv, self.stride), dtype=torch.float32, device=dev)
         self.idx = torch.empty((w.batch, w.hkv, self.k_max), dtype=torch.int32, device=dev)
+        self.kw_t = torch.zeros((w.batch,), dtype=torch.int32, device=dev)
         nv = vg.vegas_verify_workspace_size(self.kv[0], w.batch, w.gamma)
         self.ws_v = torch.zeros(max(nv, 256), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(w.head_dim)
@@ -220,6 +221,33 @@ class GpuIteration:
         w = self.w
         self.vg.vegas_select_topk(self.scores, self.stride, self.lens_t, self.kps_t, self.idx,
                                   w.batch, w.hkv, self.k_max)
+
+    # -- the "next" variants: collect-all capture, one T for all heads, window selector
+    def verify_rows(self, r, mask):
+        w = self.w
+        self.vg.vegas_verify_attn_capture_rows(
+            self.kv[r], self.qv, self.out_v, self.scores, self.stride, self.lens_t, w.batch,
+            w.gamma, mask, self.scale, self.ws_v, self.ws_v.numel())
+
+    def select_shared(self):
+        w = self.w
+        self.vg.vegas_select_topk_shared(self.scores, self.stride, self.lens_t, self.kps_t,
+                                         self.idx, w.batch, w.hkv, self.k_max)
+
+    def select_window(self):
+        w = self.w
+        # as many positions as the verification-guided selector keeps: 64 sinks + window
+        self.vg.vegas_select_window(self.lens_t, 64, self.k_max - 64, self.kw_t, self.idx,
+                                    w.batch, w.hkv, self.k_max)
+
+    def window_step(self, r):
+        w = self.w
+        self.verify(r, capture=False)
+        self.select_window()
+        for j in range(w.gamma):
+            self.vg.vegas_sparse_decode_attn(
+                self.kv[r], self.qd[j], self.out_d[j], self.idx, self.k_max, self.kw_t,
+                self.lens_t, self.tl_t[j], self.tails[j], w.batch, self.scale)
 
     def draft(self, r, j):
         w = self.w
@@ -240,6 +268,46 @@ class GpuIteration:
             self.draft(r, j)
         if ev:
             ev[3].record()
+
+
+def time_variants(it, stream, reps=100):
+    """us per call of each stage variant, each timed as a graph of `reps` calls
+    (rotating the KV replicas) replayed once after a warm replay."""
+    import torch
+    w = it.w
+    all_rows = (1 << (w.gamma + 1)) - 1
+    fns = {
+        "verify_capture2_us": lambda i: it.verify(i % it.R),
+        "verify_collect_all_us": lambda i: it.verify_rows(i % it.R, all_rows),
+        "verify_no_capture_us": lambda i: it.verify(i % it.R, capture=False),
+        "select_us": lambda i: it.select(),
+        "select_shared_us": lambda i: it.select_shared(),
+        "select_window_us": lambda i: it.select_window(),
+        "iteration_window_selector_us": lambda i: it.window_step(i % it.R),
+    }
+    out = {}
+    for name, fn in fns.items():
+        with torch.cuda.stream(stream):
+            for i in range(it.R):
+                fn(i)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                fn(i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record()
+            g.replay()
+            e1.record()
+        stream.synchronize()
+        out[name] = round(1000.0 * e0.elapsed_time(e1) / reps, 3)
+    it.vg.vegas_read_device_status(stream)
+    out["source"] = ("each variant alone in a graph of 100 calls (kernels of consecutive calls "
+                     "overlap through programmatic dependent launch)")
+    return out
 
 
 def make_events(torch, n, external):
@@ -349,7 +417,8 @@ def run_gpu(args, rank, world, dist):
                   "source": "external CUDA events at the stage boundaries of a separately "
                             "replayed graph (events there serialise the stages)"}
     e2e = run_e2e(it, stream, min(K_eff, 500), nbytes)
-    return it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e
+    variants = time_variants(it, stream)
+    return it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e, variants
 
 
 def run_e2e(it, stream, steps, nbytes):
@@ -498,8 +567,8 @@ def main():
         import torch.distributed as tdist
         tdist.init_process_group("nccl")
         dist = tdist
-    it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e = run_gpu(args, rank, world,
-                                                                              dist)
+    it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e, variants = run_gpu(
+        args, rank, world, dist)
     us_step = ms_step * 1000.0
     gbs = job_gbs(nbytes["total"], ms_step, 1)
     line = {"metric": METRIC, "value": round(job_gbs(nbytes["total"], ms_step, world), 2),
@@ -524,6 +593,9 @@ def main():
                             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                             "traffic": verify_traffic_bytes(),
                             "bytes_per_launch": nbytes["verify"]}
+    # the "next" rows, measured the same way on the same workload: collect-all
+    # capture, one T shared by all heads, the query-agnostic window selector
+    line["variants"] = variants
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ref = time_oracle(it.w, nbytes, budget_s=15.0)
         line["cpu_baseline"] = {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample")}

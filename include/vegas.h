@@ -111,6 +111,24 @@ vegas_status_t vegas_verify_attn_capture(
     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * (1'') Verify attention capturing any set of window rows.  The same call as
+ * vegas_verify_attn_capture, with the captured rows given as a bit mask
+ * (bit t set: row t, 0 <= t <= gamma) instead of two row numbers:
+ *   scores[(b * num_kv_heads + g) * score_stride + i]
+ *     = sum_{t in mask} sum_{h in group g} l_ti^(h).
+ * §2.B "Collect-2-Query" contrasts its two rows with collecting the logits of
+ * every draft row; capture_row_mask = 2^(gamma+1) - 1 is that collect-all
+ * variant.  Here every variant costs the same: the captured rows enter the
+ * kernel as one summed query (two extra MMA columns), not as logits written
+ * per row.  Needs 0 < capture_row_mask < 2^(gamma+1) when scores != NULL.
+ */
+vegas_status_t vegas_verify_attn_capture_rows(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
+    int score_stride, const int32_t* ctx_lens, int batch, int gamma,
+    uint32_t capture_row_mask, float softmax_scale, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/*
  * (1') Verify attention that allocates nothing.  The paper has no counterpart:
  * this is a convenience for callers that cannot allocate device memory, for
  * instance a plugin whose host framework owns every device allocation through
@@ -147,6 +165,34 @@ vegas_status_t vegas_select_topk(
     const float* scores, int score_stride, const int32_t* ctx_lens,
     const int32_t* k_per_seq, int32_t* out_idx, int batch, int num_kv_heads,
     int k_max, void* stream);
+
+/*
+ * (2'') One T per sequence shared by every query head: the §2.A objective with
+ * H = all query heads of the layer (the literal sum over heads) instead of the
+ * G heads of one KV head.  Same arguments and layout as vegas_select_topk; the
+ * score of position i is the fp32 sum, in KV-head order g = 0 .. Hkv-1, of
+ * scores[(b * num_kv_heads + g) * score_stride + i], and the chosen positions
+ * are written to the out_idx rows of every KV head of the sequence.
+ */
+vegas_status_t vegas_select_topk_shared(
+    const float* scores, int score_stride, const int32_t* ctx_lens,
+    const int32_t* k_per_seq, int32_t* out_idx, int batch, int num_kv_heads,
+    int k_max, void* stream);
+
+/*
+ * (2') Query-agnostic selection: the sliding-window baseline that §1
+ * "Problem" contrasts with verification-guided selection (cheap to select,
+ * poorer drafts), with optional sink positions at the start of the prefix.
+ * For every (b, g):
+ *   T_b = [0, min(num_sink, L_b)) U [max(num_sink, L_b - window), L_b),
+ * k_b = min(L_b, num_sink + window), written ascending in the layout of
+ * vegas_select_topk (entries j >= k_b set to -1), and k_out[b] = k_b (device
+ * int32 [batch]), ready for vegas_sparse_decode_attn.  Needs
+ * k_max >= num_sink + window.  ctx_lens is device int32 [batch].
+ */
+vegas_status_t vegas_select_window(const int32_t* ctx_lens, int num_sink, int window,
+                                   int32_t* k_out, int32_t* out_idx, int batch,
+                                   int num_kv_heads, int k_max, void* stream);
 
 /* ------------------------------------------------------------------------
  * (3) Sparse draft-decode attention, one draft step (§2, §3).

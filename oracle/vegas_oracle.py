@@ -177,6 +177,53 @@ def select_topk_batch(scores: np.ndarray, ctx_lens: np.ndarray, k_per_seq: np.nd
     return out
 
 
+def summed_head_scores_f32(scores_f32: np.ndarray, L: int, b: int) -> np.ndarray:
+    """s[i] = sum over the KV heads g of scores[b][g][i], i < L, added in fp32 in
+    head order g = 0, 1, ... (the precision and order the selection decision is
+    taken in on both sides)."""
+    s = np.array(scores_f32[b, 0, :L], dtype=np.float32)
+    for g in range(1, scores_f32.shape[1]):
+        s = (s + np.asarray(scores_f32[b, g, :L], dtype=np.float32)).astype(np.float32)
+    return s
+
+
+def select_topk_shared_batch(scores_f32: np.ndarray, ctx_lens: np.ndarray,
+                             k_per_seq: np.ndarray, k_max: int) -> np.ndarray:
+    """§2.A with H = every query head of the layer: one T per sequence, the k_b
+    positions of largest summed score sum_g s[b][g][i] (which equals the triple
+    sum over all heads, since each s[b][g] already sums its group's heads),
+    written to the rows of every KV head.  [B][Hkv][k_max] int32, -1 padded."""
+    B, Hkv = scores_f32.shape[0], scores_f32.shape[1]
+    out = np.full((B, Hkv, k_max), -1, dtype=np.int32)
+    for b in range(B):
+        L, k = int(ctx_lens[b]), int(k_per_seq[b])
+        T = select_topk(summed_head_scores_f32(scores_f32, L, b).astype(np.float64), k)
+        for g in range(Hkv):
+            out[b, g, :k] = T
+    return out
+
+
+def window_select(L: int, num_sink: int, window: int) -> np.ndarray:
+    """§1 "Problem": the query-agnostic sliding-window selector, with optional
+    sink positions at the start: every prefix position i in [0, L) with
+    i < num_sink or i >= L - window, ascending."""
+    return np.array([i for i in range(L) if i < num_sink or i >= L - window], dtype=np.int64)
+
+
+def window_select_batch(ctx_lens: np.ndarray, num_sink: int, window: int, num_kv_heads: int,
+                        k_max: int):
+    """(idx [B][Hkv][k_max] int32 -1 padded, k [B]) of window_select per sequence,
+    the same for every KV head."""
+    B = len(ctx_lens)
+    out = np.full((B, num_kv_heads, k_max), -1, dtype=np.int32)
+    ks = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        T = window_select(int(ctx_lens[b]), num_sink, window)
+        ks[b] = len(T)
+        out[b, :, :len(T)] = T
+    return out, ks
+
+
 # ----------------------------------------------------------------------------
 # Draft phase: sparse attention over T plus the dense tail (§2, §3)
 # ----------------------------------------------------------------------------

@@ -86,12 +86,20 @@ _verify_ws = _sig("vegas_verify_workspace_size", _sz, [_P_KV, _i32, _i32])
 _verify = _sig("vegas_verify_attn_capture", _i32,
                [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32, _i32, _i32,
                 _f32, _c_void_p, _sz, _c_void_p])
+_verify_rows = _sig("vegas_verify_attn_capture_rows", _i32,
+                    [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32,
+                     ctypes.c_uint32, _f32, _c_void_p, _sz, _c_void_p])
 _verify_noalloc = _sig("vegas_verify_attn_capture_noalloc", _i32,
                        [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32,
                         _i32, _i32, _f32, _c_void_p])
 _noalloc_max = _sig("vegas_verify_noalloc_max_scratch_bytes", _sz, [])
 _select = _sig("vegas_select_topk", _i32,
                [_c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p])
+_select_shared = _sig("vegas_select_topk_shared", _i32,
+                      [_c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32,
+                       _c_void_p])
+_window = _sig("vegas_select_window", _i32,
+               [_c_void_p, _i32, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p])
 _sparse = _sig("vegas_sparse_decode_attn", _i32,
                [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p,
                 _i32, _i32, _f32, _c_void_p])
@@ -146,6 +154,16 @@ def vegas_verify_attn_capture(kv: PagedKV, q, out, scores, score_stride: int, ct
                    _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
+def vegas_verify_attn_capture_rows(kv: PagedKV, q, out, scores, score_stride: int, ctx_lens,
+                                   batch: int, gamma: int, capture_row_mask: int,
+                                   softmax_scale: float, workspace, workspace_bytes: int,
+                                   stream=None) -> None:
+    """vegas_verify_attn_capture with the captured rows as a bit mask (bit t: row t)."""
+    _check(_verify_rows(ctypes.byref(kv), _ptr(q), _ptr(out), _ptr(scores), score_stride,
+                        _ptr(ctx_lens), batch, gamma, capture_row_mask, softmax_scale,
+                        _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
 def vegas_verify_attn_capture_noalloc(kv: PagedKV, q, out, scores, score_stride: int, ctx_lens,
                                       batch: int, gamma: int, capture_row_a: int,
                                       capture_row_b: int, softmax_scale: float,
@@ -165,6 +183,20 @@ def vegas_select_topk(scores, score_stride: int, ctx_lens, k_per_seq, out_idx, b
                       num_kv_heads: int, k_max: int, stream=None) -> None:
     _check(_select(_ptr(scores), score_stride, _ptr(ctx_lens), _ptr(k_per_seq), _ptr(out_idx),
                    batch, num_kv_heads, k_max, _stream(stream)))
+
+
+def vegas_select_topk_shared(scores, score_stride: int, ctx_lens, k_per_seq, out_idx,
+                             batch: int, num_kv_heads: int, k_max: int, stream=None) -> None:
+    """One T per sequence from the scores summed over its KV heads, written to every head."""
+    _check(_select_shared(_ptr(scores), score_stride, _ptr(ctx_lens), _ptr(k_per_seq),
+                          _ptr(out_idx), batch, num_kv_heads, k_max, _stream(stream)))
+
+
+def vegas_select_window(ctx_lens, num_sink: int, window: int, k_out, out_idx, batch: int,
+                        num_kv_heads: int, k_max: int, stream=None) -> None:
+    """The sink + sliding-window index set, in the layout of vegas_select_topk."""
+    _check(_window(_ptr(ctx_lens), num_sink, window, _ptr(k_out), _ptr(out_idx), batch,
+                   num_kv_heads, k_max, _stream(stream)))
 
 
 def vegas_sparse_decode_attn(kv: PagedKV, q, out, idx, k_max: int, k_per_seq, tail_start,

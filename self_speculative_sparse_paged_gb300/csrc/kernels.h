@@ -22,7 +22,7 @@ struct VerifyParams {
   int num_pages;
   int max_pages;
   int hq, hkv, group, gamma, nq;
-  int row_a, row_b;
+  uint32_t row_mask;        // capture rows: bit t set -> window row t is captured
   float scale;              // softmax scale (logit units)
   float scale_log2;         // scale * log2(e)
   int pages_per_split;
@@ -62,6 +62,15 @@ struct SelectParams {
   int hkv;
   int k_max;
   int chunk;                // keys per CTA of a cluster: 1, 2, 4 or 8 x select_chunk_quantum()
+  int shared;               // 1: one T per sequence from the sum over its KV heads
+  int* err;
+};
+
+struct WindowParams {
+  const int32_t* ctx_lens;
+  int32_t* k_out;           // [B]
+  int32_t* out_idx;         // [B][Hkv][k_max]
+  int num_sink, window, hkv, k_max;
   int* err;
 };
 
@@ -90,6 +99,7 @@ size_t sparse_smem_bytes(int head_dim, int ntiles);
 cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int batch,
                           cudaStream_t stream);
 
+cudaError_t launch_select_window(const WindowParams& p, int batch, cudaStream_t stream);
 int select_max_chunk();
 int select_chunk_quantum();   // a CTA's chunk is a multiple of this
 cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream);

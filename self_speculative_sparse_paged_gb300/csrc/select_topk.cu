@@ -33,6 +33,11 @@
 // its own without another exchange.  Every key > tau is taken and keys == tau
 // in position order until k are chosen; warp ballots place each chosen
 // position at its rank, so the output is ascending and deterministic.
+//
+// Shared mode (one T per sequence for every query head: the §2.A sum taken over
+// all heads instead of each KV head's group): the keys are the fp32 sums of the
+// sequence's KV-head score rows in head order, and the chosen positions are
+// written to every KV head's row.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -201,8 +206,9 @@ __device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
   }
 }
 
-// P keys per thread (the CTA's chunk is kSelThreads * P keys).
-template <int P>
+// P keys per thread (the CTA's chunk is kSelThreads * P keys); SHARED: one T per
+// sequence from the sum over its KV heads.
+template <int P, bool SHARED>
 __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelectParams p) {
   griddep_begin();
   cg::cluster_group cluster = cg::this_cluster();
@@ -229,11 +235,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   const int lim = max(0, min(p.chunk, p.score_stride - start));
   const int r0 = warp * 32 * P + lane;
   const float* src = p.scores + size_t(unit) * p.score_stride + start;
+  // one T per sequence: the fp32 sum of the sequence's KV-head rows, in head order
+  const int nsum = SHARED ? p.hkv : 1;
+  auto score_at = [&](int r) {
+    float acc = __ldcg(src + r);
+    for (int h = 1; h < nsum; ++h) acc += __ldcg(src + size_t(h) * p.score_stride + r);
+    return acc;
+  };
   float v[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = r0 + i * 32;
-    v[i] = r < lim ? __ldcg(src + r) : 0.f;
+    v[i] = r < lim ? score_at(r) : 0.f;
   }
 
   int L = p.ctx_lens[b];
@@ -243,11 +256,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     L = max(0, min(L, p.score_stride));
     k = max(0, min(k, min(L, p.k_max)));
   }
+  // output rows: this unit's, or (shared T) every KV head's row of the sequence
   int32_t* out = p.out_idx + size_t(unit) * p.k_max;
-  for (int j = k + rank * kSelThreads + tid; j < p.k_max; j += CL * kSelThreads) out[j] = -1;
+  const int nout = SHARED ? p.hkv : 1;
+  auto put = [&](int j, int32_t v) {
+    for (int h = 0; h < nout; ++h) out[size_t(h) * p.k_max + j] = v;
+  };
+  for (int j = k + rank * kSelThreads + tid; j < p.k_max; j += CL * kSelThreads) put(j, -1);
   if (k == 0) return;   // uniform over the cluster
   if (k == L) {
-    for (int j = rank * kSelThreads + tid; j < L; j += CL * kSelThreads) out[j] = j;
+    for (int j = rank * kSelThreads + tid; j < L; j += CL * kSelThreads) put(j, j);
     return;
   }
   const int nvalid = max(0, min(p.chunk, L - start));
@@ -268,7 +286,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = r0 + (u0 + i) * 32;
-        v[i] = r < nvalid ? __ldcg(src + r) : 0.f;
+        v[i] = r < nvalid ? score_at(r) : 0.f;
       }
     }
 #pragma unroll
@@ -440,8 +458,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
     const uint32_t gt_before = gt + __popc(bg & below);
     const uint32_t eq_before = eq + __popc(be & below);
-    if (is_gt) out[gt_before + min(eq_before, need)] = start + r;
-    else if (is_eq && eq_before < need) out[gt_before + eq_before] = start + r;
+    if (is_gt) put(gt_before + min(eq_before, need), start + r);
+    else if (is_eq && eq_before < need) put(gt_before + eq_before, start + r);
     gt += __popc(bg);
     eq += __popc(be);
   }
@@ -450,19 +468,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
 
 size_t select_smem_bytes(int chunk) { return size_t(kLevelWords + chunk) * 4; }
 
-template <int P>
+template <int P, bool SHARED>
 static cudaError_t launch_select_p(const SelectParams& p, int cluster, int batch,
                                    cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel<P>,
+    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel<P, SHARED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)select_smem_bytes(P * kSelThreads));
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster, p.hkv, batch);
+  cfg.gridDim = dim3(cluster, p.shared ? 1 : p.hkv, batch);
   cfg.blockDim = dim3(kSelThreads, 1, 1);
   cfg.dynamicSmemBytes = select_smem_bytes(p.chunk);
   cfg.stream = stream;
@@ -475,17 +493,24 @@ static cudaError_t launch_select_p(const SelectParams& p, int cluster, int batch
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, select_topk_kernel<P>, p);
+  return cudaLaunchKernelEx(&cfg, select_topk_kernel<P, SHARED>, p);
+}
+
+template <bool SHARED>
+static cudaError_t launch_select_s(const SelectParams& p, int cluster, int batch,
+                                   cudaStream_t stream) {
+  switch (p.chunk / kSelThreads) {
+    case 8: return launch_select_p<8, SHARED>(p, cluster, batch, stream);
+    case 16: return launch_select_p<16, SHARED>(p, cluster, batch, stream);
+    case 32: return launch_select_p<32, SHARED>(p, cluster, batch, stream);
+    case 64: return launch_select_p<64, SHARED>(p, cluster, batch, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream) {
-  switch (p.chunk / kSelThreads) {
-    case 8: return launch_select_p<8>(p, cluster, batch, stream);
-    case 16: return launch_select_p<16>(p, cluster, batch, stream);
-    case 32: return launch_select_p<32>(p, cluster, batch, stream);
-    case 64: return launch_select_p<64>(p, cluster, batch, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return p.shared ? launch_select_s<true>(p, cluster, batch, stream)
+                  : launch_select_s<false>(p, cluster, batch, stream);
 }
 
 int select_max_chunk() { return kSelMaxChunk; }

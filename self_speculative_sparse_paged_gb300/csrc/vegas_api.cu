@@ -250,10 +250,48 @@ VEGAS_API size_t vegas_verify_workspace_size(const vegas_paged_kv_t* kv, int bat
                   plan_verify(kv, batch, gamma, sms, false, dev).bytes);
 }
 
+namespace {
+vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
+                           int score_stride, const int32_t* ctx_lens, int batch, int gamma,
+                           uint32_t row_mask, float softmax_scale, void* workspace,
+                           size_t workspace_bytes, void* stream);
+}  // namespace
+
 VEGAS_API vegas_status_t vegas_verify_attn_capture(
     const vegas_paged_kv_t* kv, const void* q, void* out, float* scores, int score_stride,
     const int32_t* ctx_lens, int batch, int gamma, int capture_row_a, int capture_row_b,
     float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  uint32_t mask = 0;
+  if (scores) {
+    if (gamma < 0 || gamma > 15) return fail(VEGAS_ERR_UNSUPPORTED, "gamma %d (0..15)", gamma);
+    if (capture_row_a < 0 || capture_row_a > gamma || capture_row_b < 0 || capture_row_b > gamma)
+      return fail(VEGAS_ERR_INVALID_ARG, "capture rows (%d, %d) outside [0, %d]", capture_row_a,
+                  capture_row_b, gamma);
+    mask = (1u << capture_row_a) | (1u << capture_row_b);
+  }
+  return verify_impl(kv, q, out, scores, score_stride, ctx_lens, batch, gamma, mask,
+                     softmax_scale, workspace, workspace_bytes, stream);
+}
+
+VEGAS_API vegas_status_t vegas_verify_attn_capture_rows(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* scores, int score_stride,
+    const int32_t* ctx_lens, int batch, int gamma, uint32_t capture_row_mask,
+    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (scores) {
+    if (gamma < 0 || gamma > 15) return fail(VEGAS_ERR_UNSUPPORTED, "gamma %d (0..15)", gamma);
+    if (capture_row_mask == 0 || (capture_row_mask >> (gamma + 1)) != 0)
+      return fail(VEGAS_ERR_INVALID_ARG, "capture row mask 0x%x: needs rows in [0, %d]",
+                  capture_row_mask, gamma);
+  }
+  return verify_impl(kv, q, out, scores, score_stride, ctx_lens, batch, gamma, capture_row_mask,
+                     softmax_scale, workspace, workspace_bytes, stream);
+}
+
+namespace {
+vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
+                           int score_stride, const int32_t* ctx_lens, int batch, int gamma,
+                           uint32_t row_mask, float softmax_scale, void* workspace,
+                           size_t workspace_bytes, void* stream) {
   vegas_status_t st = check_kv(kv);
   if (st != VEGAS_OK) return st;
   if (batch < 0) return fail(VEGAS_ERR_INVALID_ARG, "batch %d", batch);
@@ -268,12 +306,8 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
     return fail(VEGAS_ERR_UNSUPPORTED,
                 "(gamma+1)*G = %d query rows (+2 capture columns) exceeds %d for head_dim %d", nq,
                 8 * vegas::verify_max_ntiles(kv->head_dim), kv->head_dim);
-  if (scores) {
-    if (score_stride < 1) return fail(VEGAS_ERR_INVALID_ARG, "score_stride %d", score_stride);
-    if (capture_row_a < 0 || capture_row_a > gamma || capture_row_b < 0 || capture_row_b > gamma)
-      return fail(VEGAS_ERR_INVALID_ARG, "capture rows (%d, %d) outside [0, %d]", capture_row_a,
-                  capture_row_b, gamma);
-  }
+  if (scores && score_stride < 1)
+    return fail(VEGAS_ERR_INVALID_ARG, "score_stride %d", score_stride);
   if (batch == 0) return VEGAS_OK;
   int* err = nullptr;
   int sms = 0;
@@ -303,8 +337,7 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   p.group = G;
   p.gamma = gamma;
   p.nq = nq;
-  p.row_a = capture_row_a;
-  p.row_b = capture_row_b;
+  p.row_mask = row_mask;
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.pages_per_split = pl.pages_per_split;
@@ -323,14 +356,15 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return VEGAS_OK;
 }
+}  // namespace
 
 // =========================================================================
 // Top-k select
 // =========================================================================
-VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride,
-                                           const int32_t* ctx_lens, const int32_t* k_per_seq,
-                                           int32_t* out_idx, int batch, int num_kv_heads,
-                                           int k_max, void* stream) {
+namespace {
+vegas_status_t select_impl(const float* scores, int score_stride, const int32_t* ctx_lens,
+                           const int32_t* k_per_seq, int32_t* out_idx, int batch,
+                           int num_kv_heads, int k_max, bool shared, void* stream) {
   if (!scores || !ctx_lens || !k_per_seq || !out_idx)
     return fail(VEGAS_ERR_INVALID_ARG, "NULL pointer argument");
   if (batch < 0 || num_kv_heads < 1 || k_max < 0 || score_stride < 1)
@@ -344,7 +378,7 @@ VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride
   int sms = 0;
   vegas_status_t st = device_info(&err, &sms);
   if (st != VEGAS_OK) return st;
-  const int units = batch * num_kv_heads;
+  const int units = batch * (shared ? 1 : num_kv_heads);
   const int quantum = vegas::select_chunk_quantum();
   auto chunk_for = [&](int c) {   // a power-of-two number of quanta
     const int ch = (score_stride + c - 1) / c;
@@ -365,9 +399,57 @@ VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride
   p.hkv = num_kv_heads;
   p.k_max = k_max;
   p.chunk = chunk_for(cl);
+  p.shared = shared ? 1 : 0;
   p.err = err;
   cudaError_t e = vegas::launch_select(p, cl, batch, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  return VEGAS_OK;
+}
+}  // namespace
+
+VEGAS_API vegas_status_t vegas_select_topk(const float* scores, int score_stride,
+                                           const int32_t* ctx_lens, const int32_t* k_per_seq,
+                                           int32_t* out_idx, int batch, int num_kv_heads,
+                                           int k_max, void* stream) {
+  return select_impl(scores, score_stride, ctx_lens, k_per_seq, out_idx, batch, num_kv_heads,
+                     k_max, false, stream);
+}
+
+VEGAS_API vegas_status_t vegas_select_topk_shared(const float* scores, int score_stride,
+                                                  const int32_t* ctx_lens,
+                                                  const int32_t* k_per_seq, int32_t* out_idx,
+                                                  int batch, int num_kv_heads, int k_max,
+                                                  void* stream) {
+  return select_impl(scores, score_stride, ctx_lens, k_per_seq, out_idx, batch, num_kv_heads,
+                     k_max, true, stream);
+}
+
+VEGAS_API vegas_status_t vegas_select_window(const int32_t* ctx_lens, int num_sink, int window,
+                                             int32_t* k_out, int32_t* out_idx, int batch,
+                                             int num_kv_heads, int k_max, void* stream) {
+  if (!ctx_lens || !k_out || !out_idx) return fail(VEGAS_ERR_INVALID_ARG, "NULL pointer argument");
+  if (batch < 0 || num_kv_heads < 1 || num_sink < 0 || window < 0 ||
+      (long long)num_sink + window > (1 << 30))
+    return fail(VEGAS_ERR_INVALID_ARG, "batch %d, num_kv_heads %d, num_sink %d, window %d", batch,
+                num_kv_heads, num_sink, window);
+  if ((long long)k_max < (long long)num_sink + window)
+    return fail(VEGAS_ERR_INVALID_ARG, "k_max %d < num_sink + window = %d", k_max,
+                num_sink + window);
+  if (batch == 0) return VEGAS_OK;
+  int* err = nullptr;
+  vegas_status_t st = device_info(&err, nullptr);
+  if (st != VEGAS_OK) return st;
+  vegas::WindowParams p{};
+  p.ctx_lens = ctx_lens;
+  p.k_out = k_out;
+  p.out_idx = out_idx;
+  p.num_sink = num_sink;
+  p.window = window;
+  p.hkv = num_kv_heads;
+  p.k_max = k_max;
+  p.err = err;
+  cudaError_t e = vegas::launch_select_window(p, batch, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "window select launch");
   return VEGAS_OK;
 }
 

@@ -170,9 +170,8 @@ __global__ void __launch_bounds__(VerifyCfg<D, NT>::W * 32, 1)
     __syncthreads();
     for (int j = tid; j < D; j += W * 32) {
       float acc = 0.f;
-      for (int r = 0; r < 2; ++r) {
-        const int t = r == 0 ? p.row_a : p.row_b;
-        if (r == 1 && p.row_b == p.row_a) break;
+      for (int t = 0; t <= p.gamma; ++t) {
+        if (!((p.row_mask >> t) & 1u)) continue;
         const __nv_bfloat16* src =
             reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t(b) * T + t) * p.hq + g * p.group) * D;
         for (int hl = 0; hl < p.group; ++hl) acc += __bfloat162float(src[hl * D + j]);

@@ -234,9 +234,8 @@ __global__ void __launch_bounds__(384, 1)
       };
       for (int j = st; j < D; j += SN) {
         float acc = 0.f;
-        for (int r = 0; r < 2; ++r) {
-          if (r == 1 && p.row_b == p.row_a) break;
-          const int t = r == 0 ? p.row_a : p.row_b;
+        for (int t = 0; t <= p.gamma; ++t) {
+          if (!((p.row_mask >> t) & 1u)) continue;
           for (int hl = 0; hl < p.group; ++hl)
             acc += __bfloat162float(
                 *reinterpret_cast<const __nv_bfloat16*>(qs + qoff(t * p.group + hl, j)));

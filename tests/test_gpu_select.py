@@ -56,3 +56,52 @@ def test_select_clustered_values():
     rng = np.random.default_rng(3)
     s = (1000.0 + rng.integers(0, 64, size=(1, 8, 32768)) * 2.0 ** -10).astype(np.float32)
     _run(s, [32768], [1639], 1639)
+
+
+# ---------------------------------------------------------------- shared T (all heads)
+def _run_shared(scores32: np.ndarray, lens, kps, k_max):
+    B, H, S = scores32.shape
+    idx = torch.full((B, H, k_max), -7, dtype=torch.int32, device=DEV)
+    vg.vegas_select_topk_shared(to_dev(scores32), S, to_dev(np.asarray(lens, np.int32)),
+                                to_dev(np.asarray(kps, np.int32)), idx, B, H, k_max)
+    vg.vegas_read_device_status()
+    ref = oracle.select_topk_shared_batch(scores32, np.asarray(lens), np.asarray(kps), k_max)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("L,k,H", [(1, 1, 8), (1000, 37, 8), (32768, 1639, 8),
+                                   (131072, 3933, 8), (5000, 250, 1)])
+def test_select_shared_random_scores(L, k, H):
+    rng = np.random.default_rng(L + 7 * k + H)
+    s = (rng.standard_normal((2, H, L)) * 3).astype(np.float32)
+    _run_shared(s, [L, L], [k, k], k + 2)
+
+
+def test_select_shared_ties_and_variable_lengths():
+    rng = np.random.default_rng(5)
+    s = rng.integers(-2, 3, size=(3, 4, 20000)).astype(np.float32)
+    _run_shared(s, [20000, 7, 15000], [900, 7, 0], 1000)
+
+
+# ---------------------------------------------------------------- sliding window (+ sinks)
+@pytest.mark.parametrize("lens,s,w", [([100, 10, 3, 0, 5000], 4, 16), ([32768], 0, 1639),
+                                      ([32768, 2000], 64, 1575), ([20, 21], 4, 16)])
+def test_select_window_matches_oracle(lens, s, w):
+    H, k_max = 3, s + w + 5
+    idx = torch.full((len(lens), H, k_max), -7, dtype=torch.int32, device=DEV)
+    ks = torch.full((len(lens),), -7, dtype=torch.int32, device=DEV)
+    vg.vegas_select_window(to_dev(np.asarray(lens, np.int32)), s, w, ks, idx, len(lens), H,
+                           k_max)
+    vg.vegas_read_device_status()
+    ref, ref_k = oracle.window_select_batch(np.asarray(lens), s, w, H, k_max)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+    np.testing.assert_array_equal(ks.cpu().numpy(), ref_k)
+
+
+def test_select_window_rejects_a_short_k_max():
+    lens = to_dev(np.asarray([100], np.int32))
+    idx = torch.zeros((1, 1, 10), dtype=torch.int32, device=DEV)
+    ks = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_select_window(lens, 4, 16, ks, idx, 1, 1, 10)
+    assert ei.value.status == 1

@@ -7,6 +7,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import oracle  # noqa: E402
+import self_speculative_sparse_paged_gb300 as vg  # noqa: E402
 from vegas_case import Case, assert_attention_close, bf16_to_f64, to_dev  # noqa: E402
 from workload import configs  # noqa: E402
 
@@ -62,3 +63,24 @@ def test_sparse_tail_only():
     ref = oracle.sparse_decode(c.qd_f64()[1], kf, vf, c.pm.block_table, idx, np.array([0]),
                                c.lens, np.array([c.w.gamma + 3]), c.scale)
     assert_attention_close(bf16_to_f64(out), ref, "tail only")
+
+
+@pytest.mark.parametrize("name,sink,window", [("qwen_b2", 4, 200), ("gptoss_b2", 0, 96),
+                                              ("tiny", 16, 4000)])
+def test_sparse_over_window_selection_matches_oracle(name, sink, window):
+    """The query-agnostic window set feeds the same draft kernel."""
+    c = Case(CASES[name])
+    w = c.w
+    k_max = sink + window
+    idx = torch.full((w.batch, w.hkv, k_max), -7, dtype=torch.int32, device="cuda")
+    ks = torch.zeros((w.batch,), dtype=torch.int32, device="cuda")
+    vg.vegas_select_window(c.lens_t, sink, window, ks, idx, w.batch, w.hkv, k_max)
+    ref_idx, ref_k = oracle.window_select_batch(c.lens, sink, window, w.hkv, k_max)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    kf, vf = c.caches_f64()
+    for j in range(w.gamma):
+        out = c.sparse(j, idx, k_per_seq=ref_k)
+        tl = w.gamma + 2 + j
+        ref = oracle.sparse_decode(c.qd_f64()[j], kf, vf, c.pm.block_table, ref_idx, ref_k,
+                                   c.lens, np.full(w.batch, tl), c.scale)
+        assert_attention_close(bf16_to_f64(out), ref, f"window draft step {j}")

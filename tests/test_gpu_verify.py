@@ -36,8 +36,10 @@ SMALL = {
 }
 
 
-def _check_case(c: Case, rows=None, capture=True):
-    out, scores = c.verify(capture=capture, rows=rows)
+def _check_case(c: Case, rows=None, capture=True, mask=None):
+    if mask is not None:
+        rows = [t for t in range(c.w.gamma + 1) if (mask >> t) & 1]
+    out, scores = c.verify(capture=capture, rows=rows, mask=mask)
     kf, vf = c.caches_f64()
     qv = c.qv_f64()
     ref_o = oracle.verify_attention(qv, kf, vf, c.pm.block_table, c.lens, c.scale)
@@ -87,6 +89,28 @@ def test_capture_switch_leaves_output_bit_identical():
 @pytest.mark.parametrize("rows", [(0, 0), (1, 4), (4, 4), (2, 3)])
 def test_capture_row_choice(rows):
     _check_case(Case(T), rows=rows)
+
+
+@pytest.mark.parametrize("name,mask", [("tiny", "all"), ("qwen_b1_ragged", "all"),
+                                       ("gptoss_b2", "all"), ("qwen_b3_var", 0b10110),
+                                       ("long_split", "all")])
+def test_capture_row_mask_matches_oracle(name, mask):
+    # collect-all (every window row) and an arbitrary row set, against the oracle's
+    # sum over the same rows; the attention output is the two-row call's, bit for bit
+    c = Case(SMALL[name])
+    m = (1 << (c.w.gamma + 1)) - 1 if mask == "all" else mask
+    out, _ = _check_case(c, mask=m)
+    out2, _ = c.verify()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_capture_row_mask_rejects_rows_past_gamma():
+    c = Case(T)
+    with pytest.raises(vg.VegasError) as ei:
+        c.verify(mask=1 << (c.w.gamma + 1))
+    assert ei.value.status == 1
+    with pytest.raises(vg.VegasError):
+        c.verify(mask=0)
 
 
 def test_repeat_calls_are_deterministic():

@@ -357,3 +357,80 @@ def test_iteration_dense_selection_reduces_to_dense_draft():
             for h in range(4):
                 ref = oracle.attention_row(qd[j, b, h], K[b, h // 2, :n], V[b, h // 2, :n], sc)
                 np.testing.assert_allclose(res["o_draft"][j, b, h], ref, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# One T shared by every query head (§2.A with H = all heads of the layer)
+# ---------------------------------------------------------------------------
+
+def test_shared_selection_is_the_all_heads_triple_sum_argmax():
+    """Brute force over subsets of the objective sum over ALL query heads (and the
+    captured rows) of the explicit dot products equals the shared selection of the
+    per-KV-head captured scores."""
+    rng = np.random.default_rng(11)
+    gamma, Hq, Hkv, d, L = 1, 4, 2, 4, 8
+    T = gamma + 1
+    q = rng.integers(-2, 3, size=(1, T, Hq, d)).astype(np.float64)
+    K = rng.integers(-2, 3, size=(Hkv, L + T, d)).astype(np.float64)
+    kc, bt = _paged(K)
+    scale = 0.5
+    s = oracle.capture_scores(q, kc, bt[None], np.array([L]), scale, rows=range(T))
+    G = Hq // Hkv
+
+    def objective(Tset):
+        return sum(scale * sum(q[0, t, h, j] * K[h // G, i, j] for j in range(d))
+                   for t in range(T) for h in range(Hq) for i in Tset)
+    for k in (1, 2, 5):
+        best = max(objective(c) for c in itertools.combinations(range(L), k))
+        idx = oracle.select_topk_shared_batch(s.astype(np.float32), np.array([L]),
+                                              np.array([k]), k)
+        assert math.isclose(objective(list(idx[0, 0, :k])), best, rel_tol=0, abs_tol=1e-9)
+        assert (idx[0] == idx[0, 0]).all()          # the same T for every KV head
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_shared_selection_ties_match_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    L = int(rng.integers(1, 10))
+    s = rng.integers(-2, 3, size=(1, 3, L)).astype(np.float32)      # exact sums, many ties
+    for k in range(0, min(L, 5) + 1):
+        idx = oracle.select_topk_shared_batch(s, np.array([L]), np.array([k]), 6)
+        assert list(idx[0, 0, :k]) == _brute_force_best(list(s[0].sum(axis=0)), k)
+        assert (idx[0, :, k:] == -1).all()
+
+
+def test_shared_selection_with_one_kv_head_is_the_per_head_selection():
+    rng = np.random.default_rng(12)
+    s = rng.standard_normal((3, 1, 40)).astype(np.float32)
+    lens, ks = np.array([40, 17, 5]), np.array([7, 17, 0])
+    np.testing.assert_array_equal(oracle.select_topk_shared_batch(s, lens, ks, 20),
+                                  oracle.select_topk_batch(s.astype(np.float64), lens, ks, 20))
+
+
+# ---------------------------------------------------------------------------
+# Query-agnostic sliding-window selector (§1 "Problem")
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L,s,w", [(100, 4, 16), (10, 4, 16), (3, 4, 16), (0, 4, 16),
+                                   (100, 0, 16), (100, 4, 0), (20, 4, 16), (21, 4, 16)])
+def test_window_selection_closed_forms(L, s, w):
+    T = oracle.window_select(L, s, w)
+    assert len(T) == min(L, s + w)
+    assert list(T) == sorted(set(T.tolist()))               # ascending, no repeats
+    if L <= s + w:
+        assert list(T) == list(range(L))                    # everything fits
+    else:
+        assert list(T) == list(range(s)) + list(range(L - w, L))
+
+
+def test_window_selection_over_the_whole_prefix_is_dense_drafting():
+    """A window covering the prefix makes the draft step the dense decode row."""
+    rng = np.random.default_rng(13)
+    q, K, V, kc, vc, bt, lens = _rand_case(rng, B=1, lens=(30,))
+    idx, ks = oracle.window_select_batch(lens, 0, 30, kc.shape[1], 32)
+    tail = np.array([3])
+    qd = rng.standard_normal((1, q.shape[2], q.shape[3]))
+    o_sparse = oracle.sparse_decode(qd, kc, vc, bt, idx, ks, lens, tail, 0.3)
+    full = np.arange(30)[None, None, :].repeat(kc.shape[1], axis=1).astype(np.int32)
+    o_full = oracle.sparse_decode(qd, kc, vc, bt, full, np.array([30]), lens, tail, 0.3)
+    np.testing.assert_allclose(o_sparse, o_full, rtol=0, atol=1e-14)

@@ -69,7 +69,8 @@ class Case:
         self.k_max = max(int(self.kps.max()), 1)
 
     # ------------------------------------------------------------ GPU calls
-    def verify(self, capture=True, rows=None, out=None, scores=None):
+    def verify(self, capture=True, rows=None, out=None, scores=None, mask=None):
+        """Verify with capture rows (a, b), or with a row bit mask when mask is given."""
         w = self.w
         rows = rows if rows is not None else (0, w.gamma)
         out = torch.empty_like(self.qv) if out is None else out
@@ -77,9 +78,14 @@ class Case:
             scores = torch.full((w.batch, w.hkv, self.stride), float("nan"), device=DEV)
         nbytes = vg.vegas_verify_workspace_size(self.kv, w.batch, w.gamma)
         ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=DEV)
-        vg.vegas_verify_attn_capture(self.kv, self.qv, out, scores if capture else None,
-                                     self.stride, self.lens_t, w.batch, w.gamma, rows[0], rows[1],
-                                     self.scale, ws, ws.numel())
+        if mask is not None:
+            vg.vegas_verify_attn_capture_rows(self.kv, self.qv, out, scores if capture else None,
+                                              self.stride, self.lens_t, w.batch, w.gamma, mask,
+                                              self.scale, ws, ws.numel())
+        else:
+            vg.vegas_verify_attn_capture(self.kv, self.qv, out, scores if capture else None,
+                                         self.stride, self.lens_t, w.batch, w.gamma, rows[0],
+                                         rows[1], self.scale, ws, ws.numel())
         return out, scores
 
     def select(self, scores, k_per_seq=None, k_max=None):
