@@ -270,6 +270,114 @@ class GpuIteration:
             ev[3].record()
 
 
+class LayerStack:
+    """`layers` attention layers of one workload shape resident in HBM, each
+    with its own paged cache and queries (the layer's generator streams) under
+    one block table, run as one decode iteration: verify(l) then select(l) for
+    every layer, then every draft step over every layer.  With `pipelined`,
+    select(l) runs on a second stream and overlaps verify(l + 1) (which does not
+    depend on it); draft step 0 of layer l waits for select(l)."""
+
+    def __init__(self, w, layers, dev):
+        import torch
+        import self_speculative_sparse_paged_gb300 as vg
+        self.torch, self.vg, self.w, self.dev, self.layers = torch, vg, w, dev, layers
+        self.lens = gen.ctx_lens(w)
+        self.kps = gen.k_per_seq(w, self.lens)
+        pm = gen.page_map(w, self.lens)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        bf = lambda a: t(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+        self.lens_t, self.kps_t, self.bt = t(self.lens), t(self.kps), t(pm.block_table)
+        need = t(gen.positions_needed(w, self.lens).astype(np.int32))
+        u, owner = t(gen.unit_direction(w)), t(pm.owner)
+        shape = (pm.num_pages, w.hkv, 16, w.head_dim)
+        self.stride = max(int(self.lens.max()), 1)
+        self.k_max = max(int(self.kps.max()), 1)
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        self.tails = [gen.tail_len(w, j) for j in range(w.gamma)]
+        self.tl_t = [torch.full((w.batch,), tl, dtype=torch.int32, device=dev) for tl in self.tails]
+        self.kv, self.qv, self.qd, self.out_v, self.out_d, self.scores, self.idx = ([] for _ in range(7))
+        self._keep = []
+        for layer in range(layers):
+            k = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+            v = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+            for which, buf in ((0, k), (1, v)):
+                vg.vegas_synth_paged_kv(buf, which, w.seed, layer, owner, pm.num_pages, w.hkv,
+                                        w.head_dim, pm.max_pages, self.lens_t, need,
+                                        gen.heavy_threshold(w), w.heavy_last, u)
+            self._keep += [k, v]
+            self.kv.append(vg.paged_kv(k, v, self.bt, w.hq))
+            self.qv.append(bf(gen.f32_to_bf16_bits(gen.verify_queries_f32(w, layer))))
+            self.qd.append(bf(gen.f32_to_bf16_bits(gen.draft_queries_f32(w, layer))))
+            self.out_v.append(torch.empty_like(self.qv[-1]))
+            self.out_d.append(torch.empty_like(self.qd[-1]))
+            self.scores.append(torch.empty((w.batch, w.hkv, self.stride), dtype=torch.float32,
+                                           device=dev))
+            self.idx.append(torch.empty((w.batch, w.hkv, self.k_max), dtype=torch.int32,
+                                        device=dev))
+        nv = vg.vegas_verify_workspace_size(self.kv[0], w.batch, w.gamma)
+        self.ws = torch.zeros(max(nv, 256), dtype=torch.uint8, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_v = [torch.cuda.Event() for _ in range(layers)]
+        self.ev_s = [torch.cuda.Event() for _ in range(layers)]
+
+    def step(self, pipelined):
+        torch, vg, w = self.torch, self.vg, self.w
+        main = torch.cuda.current_stream()
+        for layer in range(self.layers):
+            vg.vegas_verify_attn_capture(
+                self.kv[layer], self.qv[layer], self.out_v[layer], self.scores[layer],
+                self.stride, self.lens_t, w.batch, w.gamma, 0, w.gamma, self.scale, self.ws,
+                self.ws.numel(), stream=main)
+            sel_stream = self.side if pipelined else main
+            if pipelined:
+                self.ev_v[layer].record(main)
+                self.side.wait_event(self.ev_v[layer])
+            vg.vegas_select_topk(self.scores[layer], self.stride, self.lens_t, self.kps_t,
+                                 self.idx[layer], w.batch, w.hkv, self.k_max, stream=sel_stream)
+            if pipelined:
+                self.ev_s[layer].record(self.side)
+        for j in range(w.gamma):
+            for layer in range(self.layers):
+                if pipelined and j == 0:
+                    main.wait_event(self.ev_s[layer])
+                vg.vegas_sparse_decode_attn(
+                    self.kv[layer], self.qd[layer][j], self.out_d[layer][j], self.idx[layer],
+                    self.k_max, self.kps_t, self.lens_t, self.tl_t[j], self.tails[j], w.batch,
+                    self.scale, stream=main)
+
+
+def time_stack(w, layers, dev, stream, reps=10):
+    """us per iteration of a `layers`-layer stack, serial and with select(l)
+    overlapping verify(l + 1) on a second stream (each as a replayed graph)."""
+    import torch
+    st = LayerStack(w, layers, dev)
+    out = {}
+    for name, pipelined in (("serial_us", False), ("pipelined_us", True)):
+        with torch.cuda.stream(stream):
+            st.step(pipelined)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                st.step(pipelined)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record()
+            g.replay()
+            e1.record()
+        stream.synchronize()
+        out[name] = round(1000.0 * e0.elapsed_time(e1) / reps, 2)
+    st.vg.vegas_read_device_status(stream)
+    out["layers"] = layers
+    out["select_hidden_us_per_layer"] = round((out["serial_us"] - out["pipelined_us"]) / layers, 3)
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_variants(it, stream, reps=100):
     """us per call of each stage variant, each timed as a graph of `reps` calls
     (rotating the KV replicas) replayed once after a warm replay."""
@@ -418,6 +526,7 @@ def run_gpu(args, rank, world, dist):
                             "replayed graph (events there serialise the stages)"}
     e2e = run_e2e(it, stream, min(K_eff, 500), nbytes)
     variants = time_variants(it, stream)
+    variants["layer_stack_8"] = time_stack(w, 8, dev, stream)
     return it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e, variants
 
 
