@@ -206,6 +206,10 @@ class GpuIteration:
         self.scores = torch.empty((w.batch, w.hkv, self.stride), dtype=torch.float32, device=dev)
         self.idx = torch.empty((w.batch, w.hkv, self.k_max), dtype=torch.int32, device=dev)
         self.kw_t = torch.zeros((w.batch,), dtype=torch.int32, device=dev)
+        # the pages' capture: raw logits of rows {0, gamma} of every query head
+        self.raw_rows = len({0, w.gamma})
+        self.raw = torch.empty((w.batch, self.raw_rows, w.hq, self.stride), dtype=torch.float32,
+                               device=dev)
         nv = vg.vegas_verify_workspace_size(self.kv[0], w.batch, w.gamma)
         self.ws_v = torch.zeros(max(nv, 256), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(w.head_dim)
@@ -228,6 +232,18 @@ class GpuIteration:
         self.vg.vegas_verify_attn_capture_rows(
             self.kv[r], self.qv, self.out_v, self.scores, self.stride, self.lens_t, w.batch,
             w.gamma, mask, self.scale, self.ws_v, self.ws_v.numel())
+
+    def verify_raw(self, r):
+        w = self.w
+        self.vg.vegas_verify_attn_raw_logits(
+            self.kv[r], self.qv, self.out_v, self.raw, self.stride, self.lens_t, w.batch,
+            w.gamma, (1 << 0) | (1 << w.gamma), self.scale, self.ws_v, self.ws_v.numel())
+
+    def aggregate_raw(self):
+        w = self.w
+        self.vg.vegas_aggregate_raw_logits(self.raw, self.stride, self.lens_t, w.batch,
+                                           self.raw_rows, w.hq, w.hkv, self.stride, self.scores,
+                                           self.stride)
 
     def select_shared(self):
         w = self.w
@@ -388,6 +404,9 @@ def time_variants(it, stream, reps=100):
         "verify_capture2_us": lambda i: it.verify(i % it.R),
         "verify_collect_all_us": lambda i: it.verify_rows(i % it.R, all_rows),
         "verify_no_capture_us": lambda i: it.verify(i % it.R, capture=False),
+        "verify_raw_logits_us": lambda i: it.verify_raw(i % it.R),
+        "aggregate_raw_logits_us": lambda i: it.aggregate_raw(),
+        "paper_style_capture_us": lambda i: (it.verify_raw(i % it.R), it.aggregate_raw()),
         "select_us": lambda i: it.select(),
         "select_shared_us": lambda i: it.select_shared(),
         "select_window_us": lambda i: it.select_window(),

@@ -129,6 +129,30 @@ vegas_status_t vegas_verify_attn_capture_rows(
     size_t workspace_bytes, void* stream);
 
 /*
+ * (1-raw) The pages' capture, for comparison (§3 "Implementation": the verify
+ * kernel writes raw pre-softmax logits, aggregated afterwards).  Verify
+ * attention as vegas_verify_attn_capture without its fused capture, writing
+ * instead every captured row's logit of every query head:
+ *   raw[((b * R + r) * num_q_heads + h) * raw_stride + i] = l_ti^(h)
+ * for i in [0, min(L_b, raw_stride)), where t is the r-th set bit of
+ * capture_row_mask and R its popcount (device fp32).  Then
+ * vegas_aggregate_raw_logits forms the same scores as the fused capture:
+ *   scores[(b * num_kv_heads + g) * score_stride + i]
+ *     = sum_{r < num_rows} sum_{h in group g} raw[...][i],  i < L_b,
+ * summed in fp32 in (r, h) order; max_len >= max_b L_b sizes its grid.
+ * Needs L_b <= raw_stride and L_b <= score_stride for the aggregate.
+ */
+vegas_status_t vegas_verify_attn_raw_logits(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* raw, int raw_stride,
+    const int32_t* ctx_lens, int batch, int gamma, uint32_t capture_row_mask,
+    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream);
+
+vegas_status_t vegas_aggregate_raw_logits(
+    const float* raw, int raw_stride, const int32_t* ctx_lens, int batch, int num_rows,
+    int num_q_heads, int num_kv_heads, int max_len, float* scores, int score_stride,
+    void* stream);
+
+/*
  * (1') Verify attention that allocates nothing.  The paper has no counterpart:
  * this is a convenience for callers that cannot allocate device memory, for
  * instance a plugin whose host framework owns every device allocation through

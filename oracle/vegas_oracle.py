@@ -144,6 +144,28 @@ def capture_scores(q: np.ndarray, k_cache: np.ndarray, block_table: np.ndarray,
     return s
 
 
+def raw_capture_logits(q: np.ndarray, k_cache: np.ndarray, block_table: np.ndarray,
+                       ctx_lens: np.ndarray, scale: float, rows) -> np.ndarray:
+    """§3 "Implementation": the raw pre-softmax logits the pages' verify kernel
+    writes for the collected rows, raw[b][r][h][i] = l^(h)_{rows[r], i} for
+    i in [0, L_b) (0 beyond), every query head h."""
+    B, T, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    G = Hq // Hkv
+    rows = list(rows)
+    Lmax = int(np.max(ctx_lens)) if B else 0
+    raw = np.zeros((B, len(rows), Hq, Lmax), dtype=np.float64)
+    for b in range(B):
+        L = int(ctx_lens[b])
+        pos = np.arange(L, dtype=np.int64)
+        for g in range(Hkv):
+            K = gather_rows(k_cache, block_table[b], g, pos)
+            for r, t in enumerate(rows):
+                for h in range(g * G, (g + 1) * G):
+                    raw[b, r, h, :L] = logits_row(q[b, t, h], K, scale)
+    return raw
+
+
 # ----------------------------------------------------------------------------
 # Selection (§2.A): argmax over |T| = k of the summed logits
 # ----------------------------------------------------------------------------

@@ -89,6 +89,12 @@ _verify = _sig("vegas_verify_attn_capture", _i32,
 _verify_rows = _sig("vegas_verify_attn_capture_rows", _i32,
                     [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32,
                      ctypes.c_uint32, _f32, _c_void_p, _sz, _c_void_p])
+_verify_raw = _sig("vegas_verify_attn_raw_logits", _i32,
+                   [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32,
+                    ctypes.c_uint32, _f32, _c_void_p, _sz, _c_void_p])
+_raw_agg = _sig("vegas_aggregate_raw_logits", _i32,
+                [_c_void_p, _i32, _c_void_p, _i32, _i32, _i32, _i32, _i32, _c_void_p, _i32,
+                 _c_void_p])
 _verify_noalloc = _sig("vegas_verify_attn_capture_noalloc", _i32,
                        [_P_KV, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i32, _i32,
                         _i32, _i32, _f32, _c_void_p])
@@ -162,6 +168,23 @@ def vegas_verify_attn_capture_rows(kv: PagedKV, q, out, scores, score_stride: in
     _check(_verify_rows(ctypes.byref(kv), _ptr(q), _ptr(out), _ptr(scores), score_stride,
                         _ptr(ctx_lens), batch, gamma, capture_row_mask, softmax_scale,
                         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def vegas_verify_attn_raw_logits(kv: PagedKV, q, out, raw, raw_stride: int, ctx_lens,
+                                 batch: int, gamma: int, capture_row_mask: int,
+                                 softmax_scale: float, workspace, workspace_bytes: int,
+                                 stream=None) -> None:
+    """Verify writing the raw logits of the captured rows of every query head."""
+    _check(_verify_raw(ctypes.byref(kv), _ptr(q), _ptr(out), _ptr(raw), raw_stride,
+                       _ptr(ctx_lens), batch, gamma, capture_row_mask, softmax_scale,
+                       _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def vegas_aggregate_raw_logits(raw, raw_stride: int, ctx_lens, batch: int, num_rows: int,
+                               num_q_heads: int, num_kv_heads: int, max_len: int, scores,
+                               score_stride: int, stream=None) -> None:
+    _check(_raw_agg(_ptr(raw), raw_stride, _ptr(ctx_lens), batch, num_rows, num_q_heads,
+                    num_kv_heads, max_len, _ptr(scores), score_stride, _stream(stream)))
 
 
 def vegas_verify_attn_capture_noalloc(kv: PagedKV, q, out, scores, score_stride: int, ctx_lens,

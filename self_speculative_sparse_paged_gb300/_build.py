@@ -31,6 +31,7 @@ UNITS = [
     ("verify_tc.cu", "verify_tc.o", []),
     ("select_topk.cu", "select_topk.o", []),
     ("select_window.cu", "select_window.o", []),
+    ("raw_aggregate.cu", "raw_aggregate.o", []),
     ("sparse_decode.cu", "sparse_decode.o", []),
     ("verify_attn.cu", "verify_d128_c1.o", ["-DVEGAS_D=128", "-DVEGAS_CAP=1"]),
     ("verify_attn.cu", "verify_d128_c0.o", ["-DVEGAS_D=128", "-DVEGAS_CAP=0"]),

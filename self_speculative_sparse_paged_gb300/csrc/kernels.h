@@ -23,6 +23,9 @@ struct VerifyParams {
   int max_pages;
   int hq, hkv, group, gamma, nq;
   uint32_t row_mask;        // capture rows: bit t set -> window row t is captured
+  float* raw;               // raw-logit mode (no fused capture): fp32 [B][R][Hq][raw_stride], or null
+  int raw_stride;
+  int raw_rows;             // R = captured rows (popcount of row_mask) in raw mode
   float scale;              // softmax scale (logit units)
   float scale_log2;         // scale * log2(e)
   int pages_per_split;
@@ -74,6 +77,14 @@ struct WindowParams {
   int* err;
 };
 
+struct RawAggParams {
+  const float* raw;         // [B][R][Hq][raw_stride]
+  float* scores;            // [B][Hkv][score_stride]
+  const int32_t* ctx_lens;
+  int raw_stride, score_stride, rows, hq, hkv;
+  int* err;
+};
+
 // Records `msg` as this host thread's vegas_last_error_detail(); returns status.
 int record_failure(int status, const char* msg);
 
@@ -100,6 +111,8 @@ cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int b
                           cudaStream_t stream);
 
 cudaError_t launch_select_window(const WindowParams& p, int batch, cudaStream_t stream);
+cudaError_t launch_raw_aggregate(const RawAggParams& p, int batch, int max_len,
+                                 cudaStream_t stream);
 int select_max_chunk();
 int select_chunk_quantum();   // a CTA's chunk is a multiple of this
 cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream);

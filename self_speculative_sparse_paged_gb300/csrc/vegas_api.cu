@@ -254,7 +254,8 @@ namespace {
 vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
                            int score_stride, const int32_t* ctx_lens, int batch, int gamma,
                            uint32_t row_mask, float softmax_scale, void* workspace,
-                           size_t workspace_bytes, void* stream);
+                           size_t workspace_bytes, void* stream, float* raw = nullptr,
+                           int raw_stride = 0);
 }  // namespace
 
 VEGAS_API vegas_status_t vegas_verify_attn_capture(
@@ -271,6 +272,51 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
   }
   return verify_impl(kv, q, out, scores, score_stride, ctx_lens, batch, gamma, mask,
                      softmax_scale, workspace, workspace_bytes, stream);
+}
+
+VEGAS_API vegas_status_t vegas_verify_attn_raw_logits(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* raw, int raw_stride,
+    const int32_t* ctx_lens, int batch, int gamma, uint32_t capture_row_mask,
+    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!raw) return fail(VEGAS_ERR_INVALID_ARG, "NULL raw");
+  if (raw_stride < 1) return fail(VEGAS_ERR_INVALID_ARG, "raw_stride %d", raw_stride);
+  if (gamma < 0 || gamma > 15) return fail(VEGAS_ERR_UNSUPPORTED, "gamma %d (0..15)", gamma);
+  if (capture_row_mask == 0 || (capture_row_mask >> (gamma + 1)) != 0)
+    return fail(VEGAS_ERR_INVALID_ARG, "capture row mask 0x%x: needs rows in [0, %d]",
+                capture_row_mask, gamma);
+  return verify_impl(kv, q, out, nullptr, 0, ctx_lens, batch, gamma, capture_row_mask,
+                     softmax_scale, workspace, workspace_bytes, stream, raw, raw_stride);
+}
+
+VEGAS_API vegas_status_t vegas_aggregate_raw_logits(const float* raw, int raw_stride,
+                                                    const int32_t* ctx_lens, int batch,
+                                                    int num_rows, int num_q_heads,
+                                                    int num_kv_heads, int max_len,
+                                                    float* scores, int score_stride,
+                                                    void* stream) {
+  if (!raw || !ctx_lens || !scores) return fail(VEGAS_ERR_INVALID_ARG, "NULL pointer argument");
+  if (batch < 0 || num_rows < 1 || num_kv_heads < 1 || num_q_heads < num_kv_heads ||
+      num_q_heads % num_kv_heads != 0 || raw_stride < 1 || score_stride < 1 || max_len < 0)
+    return fail(VEGAS_ERR_INVALID_ARG,
+                "batch %d, rows %d, heads %d/%d, strides %d/%d, max_len %d", batch, num_rows,
+                num_q_heads, num_kv_heads, raw_stride, score_stride, max_len);
+  if (batch == 0) return VEGAS_OK;
+  int* err = nullptr;
+  vegas_status_t st = device_info(&err, nullptr);
+  if (st != VEGAS_OK) return st;
+  vegas::RawAggParams p{};
+  p.raw = raw;
+  p.scores = scores;
+  p.ctx_lens = ctx_lens;
+  p.raw_stride = raw_stride;
+  p.score_stride = score_stride;
+  p.rows = num_rows;
+  p.hq = num_q_heads;
+  p.hkv = num_kv_heads;
+  p.err = err;
+  cudaError_t e = vegas::launch_raw_aggregate(p, batch, max_len, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "raw aggregate launch");
+  return VEGAS_OK;
 }
 
 VEGAS_API vegas_status_t vegas_verify_attn_capture_rows(
@@ -291,7 +337,7 @@ namespace {
 vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
                            int score_stride, const int32_t* ctx_lens, int batch, int gamma,
                            uint32_t row_mask, float softmax_scale, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+                           size_t workspace_bytes, void* stream, float* raw, int raw_stride) {
   vegas_status_t st = check_kv(kv);
   if (st != VEGAS_OK) return st;
   if (batch < 0) return fail(VEGAS_ERR_INVALID_ARG, "batch %d", batch);
@@ -338,6 +384,9 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   p.gamma = gamma;
   p.nq = nq;
   p.row_mask = row_mask;
+  p.raw = raw;
+  p.raw_stride = raw_stride;
+  p.raw_rows = __builtin_popcount(row_mask);
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.pages_per_split = pl.pages_per_split;

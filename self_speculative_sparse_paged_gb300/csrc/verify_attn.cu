@@ -37,7 +37,7 @@ struct VerifyCfg {
   static constexpr int W = (D == 128 && P == 2) ? 6 : 8;            // warps per CTA
   static constexpr int kStages = (D == 128) ? (P == 2 ? 2 : 3) : (P == 2 ? 3 : 4);
   static constexpr size_t kStageBytes = size_t(W) * kStages * kStage;
-  static constexpr size_t kSmem = kStageBytes + size_t(NT) * 8 * (2 * D + 16) +
+  static constexpr size_t kSmem = kStageBytes + size_t(NT) * 8 * (2 * D + 16 + 4) +
                                   size_t(W) * kStages * 8 + 1024;
 };
 
@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(VerifyCfg<D, NT>::W * 32, 1)
   uint8_t* stage_area = smem;
   uint8_t* qs = smem + Cfg::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(qs + NPAD * QROW);
+  int* rawrow = reinterpret_cast<int*>(bars + W * STAGES);   // [NPAD] raw-logit row or -1
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -207,6 +208,22 @@ __global__ void __launch_bounds__(VerifyCfg<D, NT>::W * 32, 1)
     Lcap = p.score_stride;
   }
   const int last_valid = L + p.gamma;
+  // raw-logit mode: column n = t * G + hl of a captured row t goes to row
+  // (b * R + rank of t among the captured rows) * Hq + g * G + hl
+  const bool raw = !CAPTURE && p.raw != nullptr;
+  if (raw) {
+    for (int n = tid; n < NPAD; n += W * 32) {
+      int rr = -1;
+      if (n < p.nq) {
+        const int t = n / p.group, hl = n - t * p.group;
+        if ((p.row_mask >> t) & 1u)
+          rr = (b * p.raw_rows + __popc(p.row_mask & ((1u << t) - 1u))) * p.hq + g * p.group + hl;
+      }
+      rawrow[n] = rr;
+    }
+    __syncthreads();
+  }
+  const int Lraw = raw ? min(L, p.raw_stride) : 0;
 
   int done = 0;
   bool ok = true;
@@ -256,6 +273,21 @@ __global__ void __launch_bounds__(VerifyCfg<D, NT>::W * 32, 1)
             if (pa + 8 < Lcap) srow[pa + 8] = (sc[pg][nt][2] + sc[pg][nt][3]) * p.scale;
           }
       }
+    }
+    if (raw) {
+      // the pages' way: every captured row's logit of every head goes to memory
+#pragma unroll
+      for (int pg = 0; pg < P; ++pg)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int n = nt * 8 + 2 * (lane & 3) + (k & 1);
+            const int pos = pos0[pg] + (lane >> 2) + 8 * (k >> 1);
+            const int rr = rawrow[n];
+            if (live[pg] && rr >= 0 && pos < Lraw)
+              p.raw[size_t(rr) * p.raw_stride + pos] = sc[pg][nt][k] * p.scale;
+          }
     }
     float x[P][NT][4];
 #pragma unroll

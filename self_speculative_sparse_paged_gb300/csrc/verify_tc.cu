@@ -61,7 +61,7 @@ struct TcCfg {
   static constexpr int kNumBars = 2 * KS + 2 * VS + 4 * 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // misc: tmem slot, flag, votes[2][4], colmax[2][4][NQC], colsum[2][4][NQC], tlim[NQP]
-  static constexpr size_t kMisc = 16 + 32 + 4 * (16 * NQC + NQP);
+  static constexpr size_t kMisc = 16 + 32 + 4 * (16 * NQC + 2 * NQP);
   static constexpr size_t kSmem = size_t(kOffMisc) + kMisc + 1024;
 };
 
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(384, 1)
   float* colmax = reinterpret_cast<float*>(misc + 48);           // [2][4][NQC]
   float* colsum = colmax + 8 * NQC;                              // [2][4][NQC]
   int* tlim = reinterpret_cast<int*>(colsum + 8 * NQC);          // [NQP]
+  int* rawrow = tlim + NQP;                                      // [NQP] raw-logit row of a column, or -1
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -224,7 +225,18 @@ __global__ void __launch_bounds__(384, 1)
       }
       *reinterpret_cast<uint4*>(qs + (c >> 3) * (NQP * 128) + n * 128 + (((c & 7) ^ (n & 7)) << 4)) = v;
     }
-    for (int n = st; n < NQP; n += SN) tlim[n] = n < p.nq ? min(n / p.group, p.gamma) : -1;
+    for (int n = st; n < NQP; n += SN) {
+      tlim[n] = n < p.nq ? min(n / p.group, p.gamma) : -1;
+      // raw-logit mode: column n = t * G + hl of a captured row t goes to row
+      // (b * R + rank of t among the captured rows) * Hq + g * G + hl
+      int rr = -1;
+      if (!CAPTURE && p.raw && n < p.nq) {
+        const int t = n / p.group, hl = n - t * p.group;
+        if ((p.row_mask >> t) & 1u)
+          rr = (b * p.raw_rows + __popc(p.row_mask & ((1u << t) - 1u))) * p.hq + g * p.group + hl;
+      }
+      rawrow[n] = rr;
+    }
     if (CAPTURE) {
       named_bar(4, SN);
       // the summed captured query as a bf16 part and a bf16 remainder, summed
@@ -438,6 +450,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int n = 0; n < NQC; ++n)
           if (n == cap0 || n == cap0 + 1) c += x[n];
         srow[pos] = c * p.scale;
+      }
+      if (!CAPTURE && p.raw && okt && live && pos < min(L, p.raw_stride)) {
+        // the pages' way: every captured row's logit of every head goes to memory
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) {
+          const int rr = rawrow[n];
+          if (rr >= 0) p.raw[size_t(rr) * p.raw_stride + pos] = x[n] * p.scale;
+        }
       }
       const int lpos = (live ? page : pbeg + 8 * t) * 16 + (i & 15);   // position loaded in row i
       if (okt && lpos > last_valid) {

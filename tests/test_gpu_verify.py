@@ -134,3 +134,49 @@ def test_cluster_merged_shape_needs_no_workspace():
     vg.vegas_read_device_status()
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(scores[..., :5000], ref_scores[..., :5000])
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_b1_ragged", "gptoss_b2", "qwen_b3_var"])
+def test_raw_logits_and_their_aggregate_match_oracle(name):
+    """The pages' capture: raw logits of rows {0, gamma} for every query head, then
+    summed per KV head by the aggregation kernel; the attention output is the
+    capture-free verify's, bit for bit."""
+    c = Case(SMALL[name])
+    w = c.w
+    rows = sorted({0, w.gamma})
+    mask = sum(1 << t for t in rows)
+    R = len(rows)
+    raw = torch.full((w.batch, R, w.hq, c.stride), float("nan"), device="cuda")
+    out = torch.empty_like(c.qv)
+    nbytes = vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma)
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    vg.vegas_verify_attn_raw_logits(c.kv, c.qv, out, raw, c.stride, c.lens_t, w.batch, w.gamma,
+                                    mask, c.scale, ws, ws.numel())
+    scores = torch.full((w.batch, w.hkv, c.stride), float("nan"), device="cuda")
+    vg.vegas_aggregate_raw_logits(raw, c.stride, c.lens_t, w.batch, R, w.hq, w.hkv,
+                                  int(c.lens.max()), scores, c.stride)
+    vg.vegas_read_device_status()
+    plain, _ = c.verify(capture=False)
+    assert torch.equal(out.view(torch.int16), plain.view(torch.int16))
+    kf, _ = c.caches_f64()
+    qv = c.qv_f64()
+    ref_raw = oracle.raw_capture_logits(qv, kf, c.pm.block_table, c.lens, c.scale, rows)
+    ref_s = oracle.capture_scores(qv, kf, c.pm.block_table, c.lens, c.scale, rows=rows)
+    got_raw = raw.cpu().numpy().astype(np.float64)
+    got_s = scores.cpu().numpy().astype(np.float64)
+    G = w.group
+    for b in range(w.batch):
+        L = int(c.lens[b])
+        if L == 0:
+            continue
+        for g in range(w.hkv):
+            K = oracle.gather_rows(kf, c.pm.block_table[b], g, np.arange(L))
+            for r, t in enumerate(rows):
+                for h in range(g * G, (g + 1) * G):
+                    bound = score_bound(qv[b, t, h][None], K, c.scale) + 1e-30
+                    err = np.abs(got_raw[b, r, h, :L] - ref_raw[b, r, h, :L])
+                    assert np.all(err <= bound), f"raw logit error {err.max()} (b={b} h={h})"
+            qr = np.concatenate([qv[b, t, g * G:(g + 1) * G] for t in rows])
+            bound = score_bound(qr, K, c.scale) + 1e-30
+            err = np.abs(got_s[b, g, :L] - ref_s[b, g, :L])
+            assert np.all(err <= bound), f"aggregated score error {err.max()} (b={b}, g={g})"

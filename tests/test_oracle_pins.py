@@ -434,3 +434,22 @@ def test_window_selection_over_the_whole_prefix_is_dense_drafting():
     full = np.arange(30)[None, None, :].repeat(kc.shape[1], axis=1).astype(np.int32)
     o_full = oracle.sparse_decode(qd, kc, vc, bt, full, np.array([30]), lens, tail, 0.3)
     np.testing.assert_allclose(o_sparse, o_full, rtol=0, atol=1e-14)
+
+
+def test_raw_logits_sum_to_the_capture_and_match_dot_products():
+    """§3's raw logits: explicit dot products entry by entry, and their sum over the
+    rows and the group's heads is the (brute-force-pinned) capture."""
+    rng = np.random.default_rng(14)
+    q, K, V, kc, vc, bt, lens = _rand_case(rng, B=2, lens=(21, 37))
+    rows = (0, 3)
+    raw = oracle.raw_capture_logits(q, kc, bt, lens, 0.25, rows)
+    G = q.shape[2] // kc.shape[1]
+    for b in range(2):
+        L = int(lens[b])
+        for r, t in enumerate(rows):
+            for h in range(q.shape[2]):
+                want = [0.25 * float(np.dot(q[b, t, h], K[b, h // G, i])) for i in range(L)]
+                np.testing.assert_allclose(raw[b, r, h, :L], want, rtol=0, atol=1e-12)
+    s = oracle.capture_scores(q, kc, bt, lens, 0.25, rows=rows)
+    agg = raw.reshape(2, len(rows), kc.shape[1], G, -1).sum(axis=(1, 3))
+    np.testing.assert_allclose(agg, s, rtol=0, atol=1e-12)
