@@ -15,8 +15,8 @@
 // groups with one 1-D bulk copy per K row and per V row (lanes 0-15 K, 16-31
 // V) into padded rows and runs the same warp core as the verify kernel with
 // the G query heads of the group as the tile's columns.  The CTAs' softmax
-// states meet in distributed shared memory: rank 0 merges them and writes the
-// output, with no global scratch and no second pass.
+// states meet in distributed shared memory: each CTA merges a slice of the
+// output elements and writes it, with no global scratch and no second pass.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -43,7 +43,6 @@ constexpr size_t sparse_smem_layout_bytes() {
          + size_t(kAttnWarps) * SparseCfg<D>::kStages * 8          // mbarriers
          + size_t(SparseCfg<D>::kMaxRows) * 4                      // row table
          + size_t(NT) * 8 * (D + 2) * 4                            // CTA partial
-         + size_t(kMaxSparseCluster) * NT * 8 * 4                  // rank-0 weights
          + 1024;
 }
 
@@ -74,7 +73,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   float* pM = reinterpret_cast<float*>(rows + SparseCfg<D>::kMaxRows);   // [NPAD] CTA partial
   float* pL = pM + NPAD;                                                 // [NPAD]
   float* pO = pL + NPAD;                                                 // [NPAD][D]
-  float* wts = pO + NPAD * D;                                            // [8][NPAD] rank-0 weights
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -92,6 +90,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   const int rbeg = rank * p.rows_per_split;
   const int rend = min(rbeg + p.rows_per_split, total);
   const int nrows = max(0, rend - rbeg);
+
+  // The draft queries are requested first, so their load overlaps the index
+  // and block-table loads below (one 16-byte chunk per thread).
+  constexpr int QCH = NPAD * (D / 8);
+  static_assert(QCH <= NTH, "one Q chunk per thread");
+  uint4 qchunk = make_uint4(0, 0, 0, 0);
+  if (tid < QCH && tid / (D / 8) < p.group)
+    qchunk = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                            (size_t(b) * p.hq + g * p.group + tid / (D / 8)) * D)
+        [tid % (D / 8)];
 
   if (tid == 0) {
     // one arrival per lane per stage use: each lane's cp.async copies signal it
@@ -130,16 +138,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
       }
     }
   }
-  for (int i = tid; i < NPAD * (D / 8); i += NTH) {
-    const int n = i / (D / 8), c = i % (D / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (n < p.group) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t(b) * p.hq + g * p.group + n) * D);
-      v = src[c];
-    }
-    *reinterpret_cast<uint4*>(qs + n * QROW + c * 16) = v;
-  }
+  if (tid < QCH)
+    *reinterpret_cast<uint4*>(qs + (tid / (D / 8)) * QROW + (tid % (D / 8)) * 16) = qchunk;
   __syncthreads();
 
   const int ngroups = (nrows + 15) / 16;
@@ -216,45 +216,44 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   __syncthreads();
   cta_merge_to_smem<D, NT, W>(st, stage_area, SparseCfg<D>::kStageBytes, p.group, pM, pL, pO);
 
-  // Cluster merge: rank 0 weighs every CTA's state through distributed shared
-  // memory, M = max_r m_r, w_r = 2^(m_r - M) / sum_r 2^(m_r - M) l_r.
+  // Cluster merge: every CTA merges a slice of the G x D output elements,
+  // reading every CTA's state through distributed shared memory in one round
+  // trip: M = max_r m_r, O = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r.
   cluster.sync();
-  if (rank == 0) {
+  {
     constexpr int R = kMaxSparseCluster;   // remote loads are issued together, unrolled
-    for (int n = tid; n < p.group; n += NTH) {
-      float mr[R], lr[R];
+    const int nel = p.group * D;
+    const int per = (nel + CL - 1) / CL;
+    const int e0 = rank * per, e1 = min(nel, e0 + per);
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    for (int e = e0 + tid; e < e1; e += NTH) {
+      const int n = e / D;
+      float mr[R], lr[R], v[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        mr[r] = r < CL ? cluster.map_shared_rank(pM, r)[n] : -INFINITY;
-        lr[r] = r < CL ? cluster.map_shared_rank(pL, r)[n] : 0.f;
+        mr[r] = -INFINITY;
+        lr[r] = v[r] = 0.f;
+        if (r < CL) {
+          mr[r] = cluster.map_shared_rank(pM, r)[n];
+          lr[r] = cluster.map_shared_rank(pL, r)[n];
+          v[r] = cluster.map_shared_rank(pO, r)[e];
+        }
       }
       float M = -INFINITY;
 #pragma unroll
       for (int r = 0; r < R; ++r) M = fmaxf(M, mr[r]);
-      float L = 0.f;
+      float L = 0.f, a = 0.f;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        mr[r] = r < CL ? ex2(mr[r] - M) : 0.f;
-        L += mr[r] * lr[r];
+        const float f = r < CL ? ex2(mr[r] - M) : 0.f;
+        L += f * lr[r];
+        a += f * v[r];
       }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int r = 0; r < R; ++r) wts[r * NPAD + n] = mr[r] * inv;
-    }
-    __syncthreads();
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-    for (int e = tid; e < p.group * D; e += NTH) {
-      const int n = e / D;
-      float v[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) v[r] = r < CL ? cluster.map_shared_rank(pO, r)[e] : 0.f;
-      float a = 0.f;
-#pragma unroll
-      for (int r = 0; r < R; ++r) a += wts[r * NPAD + n] * v[r];
-      out[(size_t(b) * p.hq + g * p.group + n) * D + (e % D)] = __float2bfloat16_rn(a);
+      out[(size_t(b) * p.hq + g * p.group + n) * D + (e % D)] =
+          __float2bfloat16_rn(L > 0.f ? a / L : 0.f);
     }
   }
-  cluster.sync();   // no CTA leaves while rank 0 may still read its shared memory
+  cluster.sync();   // no CTA leaves while another may still read its shared memory
 }
 
 template <int D, int NT>

@@ -227,15 +227,17 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int n = st; n < NQP; n += SN) {
       tlim[n] = n < p.nq ? min(n / p.group, p.gamma) : -1;
-      // raw-logit mode: column n = t * G + hl of a captured row t goes to row
-      // (b * R + rank of t among the captured rows) * Hq + g * G + hl
-      int rr = -1;
-      if (!CAPTURE && p.raw && n < p.nq) {
-        const int t = n / p.group, hl = n - t * p.group;
-        if ((p.row_mask >> t) & 1u)
-          rr = (b * p.raw_rows + __popc(p.row_mask & ((1u << t) - 1u))) * p.hq + g * p.group + hl;
+      if constexpr (!CAPTURE) {
+        // raw-logit mode: column n = t * G + hl of a captured row t goes to row
+        // (b * R + rank of t among the captured rows) * Hq + g * G + hl
+        int rr = -1;
+        if (p.raw && n < p.nq) {
+          const int t = n / p.group, hl = n - t * p.group;
+          if ((p.row_mask >> t) & 1u)
+            rr = (b * p.raw_rows + __popc(p.row_mask & ((1u << t) - 1u))) * p.hq + g * p.group + hl;
+        }
+        rawrow[n] = rr;
       }
-      rawrow[n] = rr;
     }
     if (CAPTURE) {
       named_bar(4, SN);
