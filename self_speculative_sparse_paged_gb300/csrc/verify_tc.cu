@@ -72,20 +72,19 @@ constexpr int kTcStateFloats = NQC * 128 + 2 * NQC;
 
 // Split-KV merge on chip, when the num_splits CTAs of a (sequence, KV head)
 // unit form one thread-block cluster (rank = split; a single split is a
-// cluster of one).  Each CTA has staged the states of its two softmax groups
-// in shared memory at `st` (kTcStateFloats apart).  After a cluster barrier,
-// CTA r merges rows n = r, r + S, ... over the 2 S states read through
-// distributed shared memory (merge rule as in split_merge.cuh), writes bf16
-// rows, and leaves only once no CTA reads its shared memory any more.  Called
-// by every thread of every CTA of the cluster.
+// cluster of one).  Each CTA has staged its state (its two softmax groups
+// already merged) in shared memory at `st`.  After a cluster barrier, CTA r
+// merges rows n = r, r + S, ... over the S states read through distributed
+// shared memory (merge rule as in split_merge.cuh), writes bf16 rows, and
+// leaves only once no CTA reads its shared memory any more.  Called by every
+// thread of every CTA of the cluster.
 template <int NQC, class OutRow>
 __device__ __forceinline__ void cluster_merge_rows(const float* st, int S, int nq, OutRow out_row) {
   constexpr int D = 128;
-  constexpr int SF = kTcStateFloats<NQC>;
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int r = (int)cluster.block_rank(), tid = threadIdx.x;
-  const int nstates = 2 * S;
+  const int nstates = S;
   if (tid < 2 * D) {
     const int d = tid & (D - 1);
     for (int n = r + (tid >> 7) * S; n < nq; n += 2 * S) {
@@ -97,7 +96,7 @@ __device__ __forceinline__ void cluster_merge_rows(const float* st, int S, int n
         for (int j = 0; j < 8; ++j) {
           const int sidx = s0 + j;
           if (sidx < nstates) {
-            const float* rs = cluster.map_shared_rank(st, sidx >> 1) + (sidx & 1) * SF;
+            const float* rs = cluster.map_shared_rank(st, sidx);
             os[j] = rs[n * D + d];
             ms[j] = rs[NQC * D + n];
             ls[j] = rs[NQC * D + NQC + n];
@@ -623,8 +622,27 @@ __global__ void __launch_bounds__(384, 1)
       return out + ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D;
     };
     if (p.cluster_merge || p.num_splits == 1) {
-      // (one split: a cluster of one CTA merging its two group states)
-      cluster_merge_rows<NQC>(reinterpret_cast<const float*>(smem), p.num_splits, p.nq, out_row);
+      // The CTA's two group states merge in place into state 0 first (shared
+      // memory only), so the cluster merge reads one state per CTA.
+      constexpr int SF = kTcStateFloats<NQC>;
+      float* st0 = reinterpret_cast<float*>(smem);
+      const float* st1 = st0 + SF;
+      for (int e = tid; e < p.nq * D; e += Cfg::kThreads) {
+        const int n = e / D;
+        const float m0 = st0[NQC * D + n], m1 = st1[NQC * D + n];
+        const float M = fmaxf(m0, m1);
+        st0[e] = ex2(m0 - M) * st0[e] + ex2(m1 - M) * st1[e];
+      }
+      __syncthreads();   // every element read the maxima before they change
+      if (tid < p.nq) {
+        const float m0 = st0[NQC * D + tid], m1 = st1[NQC * D + tid];
+        const float M = fmaxf(m0, m1);
+        st0[NQC * D + NQC + tid] =
+            ex2(m0 - M) * st0[NQC * D + NQC + tid] + ex2(m1 - M) * st1[NQC * D + NQC + tid];
+        st0[NQC * D + tid] = M;
+      }
+      // (one split: a cluster of one CTA)
+      cluster_merge_rows<NQC>(st0, p.num_splits, p.nq, out_row);
     } else {
       SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
       finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, 2 * p.num_splits, p.nq, out_row,
