@@ -62,7 +62,7 @@ VERIFY_TRAFFIC = {
     "bytes": 135_610_000,
     "sources": ["verify_tc.cu", "split_merge.cuh", "attn_core.cuh", "vegas_common.cuh",
                 "kernels.h"],
-    "sha256": "5eb465366f7f08dd83456c3a1838bc0c3a407a03633fcb92d0bdb9eeba10363b",
+    "sha256": "a2d4a09241e3b7c3417cdba99aaf6a22cb9e036522d14bf299163f9d42d8e908",
 }
 
 
