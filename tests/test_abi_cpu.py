@@ -79,3 +79,40 @@ def test_host_validation_rejects_before_launch(vg):
     with pytest.raises(vg.VegasError) as ei:
         vg.vegas_select_topk(16, 16 * 32768 + 1, 16, 16, 16, 1, 8, 10, stream=0)
     assert ei.value.status == 2
+
+
+def test_host_validation_of_the_variant_entry_points(vg):
+    kv = vg.PagedKV(16, 16, 16, 4, 16, 8, 2, 64, 4)
+    # capture row masks must name rows inside [0, gamma]
+    for mask in (0, 1 << 5):
+        with pytest.raises(vg.VegasError) as ei:
+            vg.vegas_verify_attn_capture_rows(kv, 16, 16, 16, 64, 16, 1, 4, mask, 0.125, None, 0,
+                                              stream=0)
+        assert ei.value.status == 1
+    # raw-logit mode needs a buffer and a valid mask
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_raw_logits(kv, 16, 16, None, 64, 16, 1, 4, 0b10001, 0.125, None, 0,
+                                        stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_raw_logits(kv, 16, 16, 16, 64, 16, 1, 4, 1 << 7, 0.125, None, 0,
+                                        stream=0)
+    assert ei.value.status == 1
+    # aggregate: query heads must be a multiple of the KV heads
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_aggregate_raw_logits(16, 64, 16, 1, 2, 6, 4, 64, 16, 64, stream=0)
+    assert ei.value.status == 1
+    # window selection needs k_max >= sinks + window
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_select_window(16, 4, 16, 16, 16, 1, 2, 10, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_select_window(16, -1, 16, 16, 16, 1, 2, 20, stream=0)
+    assert ei.value.status == 1
+    # shared select: same argument checks as the per-head select
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_select_topk_shared(None, 64, 16, 16, 16, 1, 2, 8, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_select_topk_shared(16, 9 * 32768, 16, 16, 16, 1, 2, 8, stream=0)
+    assert ei.value.status == 2
