@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace vegas {
 
 constexpr int kAttnWarps = 8;          // warps per attention CTA
@@ -84,6 +86,21 @@ struct RawAggParams {
   int raw_stride, score_stride, rows, hq, hkv;
   int* err;
 };
+
+// Runs f() (a kernel-attribute setter, which acts on the current device) once
+// per device: `done` holds one bit per device ordinal below 32.  Two threads
+// racing on a device may both run f, which is harmless for attribute setters.
+template <class F>
+inline cudaError_t once_per_device(std::atomic<uint32_t>& done, F&& f) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint32_t bit = (dev >= 0 && dev < 32) ? (1u << dev) : 0u;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = f();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Records `msg` as this host thread's vegas_last_error_detail(); returns status.
 int record_failure(int status, const char* msg);

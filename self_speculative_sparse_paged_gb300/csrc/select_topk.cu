@@ -471,14 +471,13 @@ size_t select_smem_bytes(int chunk) { return size_t(kLevelWords + chunk) * 4; }
 template <int P, bool SHARED>
 static cudaError_t launch_select_p(const SelectParams& p, int cluster, int batch,
                                    cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel<P, SHARED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)select_smem_bytes(P * kSelThreads));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint32_t> configured{0};
+  cudaError_t e = once_per_device(configured, [] {
+    return cudaFuncSetAttribute(select_topk_kernel<P, SHARED>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)select_smem_bytes(P * kSelThreads));
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, p.shared ? 1 : p.hkv, batch);
   cfg.blockDim = dim3(kSelThreads, 1, 1);

@@ -259,13 +259,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
 template <int D, int NT>
 static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStream_t stream) {
   constexpr size_t smem = sparse_smem_layout_bytes<D, NT>();
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<D, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint32_t> configured{0};
+  cudaError_t e = once_per_device(configured, [] {
+    return cudaFuncSetAttribute(sparse_decode_kernel<D, NT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits, p.hkv, batch);
   cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);

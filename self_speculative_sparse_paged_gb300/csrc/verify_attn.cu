@@ -341,14 +341,12 @@ template <int D, int NT, bool CAP>
 static cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap,
                               const VerifyParams& p, int batch, cudaStream_t stream) {
   using Cfg = VerifyCfg<D, NT>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(verify_attn_kernel<D, NT, CAP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg::kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint32_t> configured{0};
+  cudaError_t e = once_per_device(configured, [] {
+    return cudaFuncSetAttribute(verify_attn_kernel<D, NT, CAP>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits, p.hkv, batch);
   cfg.blockDim = dim3(Cfg::W * 32, 1, 1);

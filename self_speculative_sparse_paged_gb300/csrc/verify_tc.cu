@@ -654,18 +654,15 @@ __global__ void __launch_bounds__(384, 1)
 template <int NQP, int NQC, bool CAP>
 static cudaError_t configure_tc() {
   using Cfg = TcCfg<NQP, NQC>;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<uint32_t> configured{0};
+  return once_per_device(configured, [] {
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<NQP, NQC, CAP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(verify_tc_kernel<NQP, NQC, CAP>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  return cudaSuccess;
+    return cudaFuncSetAttribute(verify_tc_kernel<NQP, NQC, CAP>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
 }
 
 // Launch (launch = true) or, with launch = false, the number of clusters of
@@ -717,10 +714,15 @@ cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
 
 int verify_tc_max_active_clusters(int ncols, bool capture, int cluster) {
   if (cluster < 1 || cluster > kMaxVerifyCluster) return 0;
-  static int cache[2][5][kMaxVerifyCluster + 1];   // [capture][column tiles][cluster]
+  constexpr int kDevices = 32;
+  // [device][capture][column tiles][cluster]: 0 unknown, -1 none, else the count
+  static std::atomic<int> cache[kDevices][2][5][kMaxVerifyCluster + 1];
   const int ct = (ncols + 7) / 8;
   if (ct < 1 || ct > 4) return 0;
-  int& c = cache[capture ? 1 : 0][ct][cluster];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return 0;
+  std::atomic<int>& slot = cache[dev][capture ? 1 : 0][ct][cluster];
+  int c = slot.load(std::memory_order_acquire);
   if (c == 0) {
     VerifyParams p{};
     p.hkv = 1;
@@ -735,6 +737,7 @@ int verify_tc_max_active_clusters(int ncols, bool capture, int cluster) {
       n = 0;
     }
     c = n > 0 ? n : -1;
+    slot.store(c, std::memory_order_release);
   }
   return c > 0 ? c : 0;
 }
