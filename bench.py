@@ -62,7 +62,7 @@ VERIFY_TRAFFIC = {
     "bytes": 135_610_000,
     "sources": ["verify_tc.cu", "split_merge.cuh", "attn_core.cuh", "vegas_common.cuh",
                 "kernels.h"],
-    "sha256": "a2d4a09241e3b7c3417cdba99aaf6a22cb9e036522d14bf299163f9d42d8e908",
+    "sha256": "cda3b52cbb1668041898476bb299e8b0e257208534ee505b1f1c33cd3ef159e3",
 }
 
 
