@@ -333,9 +333,30 @@ class LayerStack:
                                         device=dev))
         nv = vg.vegas_verify_workspace_size(self.kv[0], w.batch, w.gamma)
         self.ws = torch.zeros(max(nv, 256), dtype=torch.uint8, device=dev)
+        self.kw_t = torch.zeros((w.batch,), dtype=torch.int32, device=dev)
         self.side = torch.cuda.Stream(device=dev)
         self.ev_v = [torch.cuda.Event() for _ in range(layers)]
         self.ev_s = [torch.cuda.Event() for _ in range(layers)]
+
+    def step_without_capture(self):
+        """The same iteration with verify's capture off and the query-agnostic
+        window selector (64 sinks + a window, as many positions as k): the
+        denominator of the capture-plus-select overhead."""
+        torch, vg, w = self.torch, self.vg, self.w
+        main = torch.cuda.current_stream()
+        for layer in range(self.layers):
+            vg.vegas_verify_attn_capture(
+                self.kv[layer], self.qv[layer], self.out_v[layer], None, self.stride,
+                self.lens_t, w.batch, w.gamma, 0, w.gamma, self.scale, self.ws, self.ws.numel(),
+                stream=main)
+            vg.vegas_select_window(self.lens_t, 64, self.k_max - 64, self.kw_t, self.idx[layer],
+                                   w.batch, w.hkv, self.k_max, stream=main)
+        for j in range(w.gamma):
+            for layer in range(self.layers):
+                vg.vegas_sparse_decode_attn(
+                    self.kv[layer], self.qd[layer][j], self.out_d[layer][j], self.idx[layer],
+                    self.k_max, self.kw_t, self.lens_t, self.tl_t[j], self.tails[j], w.batch,
+                    self.scale, stream=main)
 
     def step(self, pipelined):
         torch, vg, w = self.torch, self.vg, self.w
@@ -369,14 +390,16 @@ def time_stack(w, layers, dev, stream, reps=10):
     import torch
     st = LayerStack(w, layers, dev)
     out = {}
-    for name, pipelined in (("serial_us", False), ("pipelined_us", True)):
+    runs = (("serial_us", lambda: st.step(False)), ("pipelined_us", lambda: st.step(True)),
+            ("no_capture_window_select_us", st.step_without_capture))
+    for name, fn in runs:
         with torch.cuda.stream(stream):
-            st.step(pipelined)
+            fn()
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for _ in range(reps):
-                st.step(pipelined)
+                fn()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -389,6 +412,9 @@ def time_stack(w, layers, dev, stream, reps=10):
     st.vg.vegas_read_device_status(stream)
     out["layers"] = layers
     out["select_hidden_us_per_layer"] = round((out["serial_us"] - out["pipelined_us"]) / layers, 3)
+    # capture + verification-guided select over the query-agnostic baseline, pipelined
+    out["capture_plus_select_overhead_pipelined"] = round(
+        out["pipelined_us"] / out["no_capture_window_select_us"] - 1.0, 4)
     del st
     torch.cuda.empty_cache()
     return out
