@@ -252,8 +252,9 @@ class GpuIteration:
 
     def select_window(self):
         w = self.w
-        # as many positions as the verification-guided selector keeps: 64 sinks + window
-        self.vg.vegas_select_window(self.lens_t, 64, self.k_max - 64, self.kw_t, self.idx,
+        # as many positions as the verification-guided selector keeps: sinks + window
+        sinks = min(64, self.k_max // 2)
+        self.vg.vegas_select_window(self.lens_t, sinks, self.k_max - sinks, self.kw_t, self.idx,
                                     w.batch, w.hkv, self.k_max)
 
     def window_step(self, r):
@@ -340,7 +341,7 @@ class LayerStack:
 
     def step_without_capture(self):
         """The same iteration with verify's capture off and the query-agnostic
-        window selector (64 sinks + a window, as many positions as k): the
+        window selector (up to 64 sinks + a window, as many positions as k): the
         denominator of the capture-plus-select overhead."""
         torch, vg, w = self.torch, self.vg, self.w
         main = torch.cuda.current_stream()
@@ -349,8 +350,9 @@ class LayerStack:
                 self.kv[layer], self.qv[layer], self.out_v[layer], None, self.stride,
                 self.lens_t, w.batch, w.gamma, 0, w.gamma, self.scale, self.ws, self.ws.numel(),
                 stream=main)
-            vg.vegas_select_window(self.lens_t, 64, self.k_max - 64, self.kw_t, self.idx[layer],
-                                   w.batch, w.hkv, self.k_max, stream=main)
+            sinks = min(64, self.k_max // 2)
+            vg.vegas_select_window(self.lens_t, sinks, self.k_max - sinks, self.kw_t,
+                                   self.idx[layer], w.batch, w.hkv, self.k_max, stream=main)
         for j in range(w.gamma):
             for layer in range(self.layers):
                 vg.vegas_sparse_decode_attn(

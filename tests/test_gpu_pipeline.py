@@ -46,3 +46,18 @@ def test_pipelined_stack_equals_serial_and_single_layers(w, layers):
     for j in range(w.gamma):
         o = c.sparse(j, idx)
         assert torch.equal(o.view(torch.int16), pip[1][-1][j].view(torch.int16))
+
+
+def test_stack_schedule_without_capture_runs_the_window_selector():
+    """The overhead denominator: plain verify, window selection, the same drafts."""
+    w = configs.TINY
+    st = bench.LayerStack(w, 2, torch.device("cuda"))
+    st.step_without_capture()
+    torch.cuda.synchronize()
+    sinks = min(64, st.k_max // 2)
+    for layer in range(2):
+        idx = st.idx[layer].cpu().numpy()
+        L = int(st.lens[0])
+        want = [i for i in range(L) if i < sinks or i >= L - (st.k_max - sinks)]
+        assert list(idx[0, 0, :len(want)]) == want
+        assert np.isfinite(st.out_d[layer].float().cpu().numpy()).all()
