@@ -248,9 +248,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn_major, 
 // global memory it waits until that kernel has completed and its writes are
 // visible, and it lets the next kernel start launching right away.  Without
 // the launch attribute both are no-ops.
-__device__ __forceinline__ void griddep_begin() {
+__device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_begin() {
+  griddep_launch_dependents();
+  griddep_wait();
+}
+
+// Distributed shared memory: the address of the same shared-memory location
+// in the CTA of cluster rank `rank`, and a store to such an address.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // True in exactly one lane of the (fully active) warp.

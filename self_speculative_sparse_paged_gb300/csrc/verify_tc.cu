@@ -30,8 +30,9 @@
 // buffer that the PV MMA reads.
 //
 // Splits of a unit merge either on chip, when all of them form one
-// thread-block cluster (distributed shared memory, no workspace), or through
-// the workspace in the last-arriving CTA.
+// thread-block cluster (every group pushes its state to the rank that owns the
+// output row, through distributed shared memory; no workspace), or through the
+// workspace in the last-arriving CTA.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -65,64 +66,9 @@ struct TcCfg {
   static constexpr size_t kSmem = size_t(kOffMisc) + kMisc + 1024;
 };
 
-// Floats of one staged partial state: O[n][d] (unnormalised, NQC x 128), then
-// M[NQC] (running maxima, log2 units) and L[NQC] (row sums).
-template <int NQC>
-constexpr int kTcStateFloats = NQC * 128 + 2 * NQC;
-
-// Split-KV merge on chip, when the num_splits CTAs of a (sequence, KV head)
-// unit form one thread-block cluster (rank = split; a single split is a
-// cluster of one).  Each CTA has staged its state (its two softmax groups
-// already merged) in shared memory at `st`.  After a cluster barrier, CTA r
-// merges rows n = r, r + S, ... over the S states read through distributed
-// shared memory (merge rule as in split_merge.cuh), writes bf16 rows, and
-// leaves only once no CTA reads its shared memory any more.  Called by every
-// thread of every CTA of the cluster.
-template <int NQC, class OutRow>
-__device__ __forceinline__ void cluster_merge_rows(const float* st, int S, int nq, OutRow out_row) {
-  constexpr int D = 128;
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
-  const int r = (int)cluster.block_rank(), tid = threadIdx.x;
-  const int nstates = S;
-  if (tid < 2 * D) {
-    const int d = tid & (D - 1);
-    for (int n = r + (tid >> 7) * S; n < nq; n += 2 * S) {
-      // eight states' loads in flight at a time, merged into a running state
-      float M = kEmptyMax, Lsum = 0.f, O = 0.f;
-      for (int s0 = 0; s0 < nstates; s0 += 8) {
-        float ms[8], ls[8], os[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int sidx = s0 + j;
-          if (sidx < nstates) {
-            const float* rs = cluster.map_shared_rank(st, sidx);
-            os[j] = rs[n * D + d];
-            ms[j] = rs[NQC * D + n];
-            ls[j] = rs[NQC * D + NQC + n];
-          } else {
-            os[j] = ls[j] = 0.f;
-            ms[j] = kEmptyMax;
-          }
-        }
-        float Mn = M;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, ms[j]);
-        const float f = ex2(M - Mn);
-        Lsum *= f;
-        O *= f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float fj = ex2(ms[j] - Mn);
-          Lsum += fj * ls[j];
-          O += fj * os[j];
-        }
-        M = Mn;
-      }
-      out_row(n)[d] = __float2bfloat16_rn(Lsum > 0.f ? O / Lsum : 0.f);
-    }
-  }
-  // no CTA leaves while another may still read its shared memory
+// Cluster-wide barrier of every thread (release / acquire): shared-memory
+// writes before it, local or remote, are visible to every CTA after it.
+__device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -138,7 +84,7 @@ __global__ void __launch_bounds__(384, 1)
   static_assert(NQP == 16 || NQP == 32, "MMA N");
   static_assert(NQC % 8 == 0 && NQC <= NQP, "processed columns");
 
-  griddep_begin();
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -171,17 +117,6 @@ __global__ void __launch_bounds__(384, 1)
   const int unit = b * p.hkv + g;
   const int T = p.gamma + 1;
   const int cap = p.max_pages * 16;
-  int L = p.ctx_lens[b];
-  if (L < 0 || L + T > cap) {
-    if (tid == 0) set_error(p.err, kErrDeviceFault);
-    L = max(0, min(L, cap - T));
-  }
-  const int npages = (L + T + 15) / 16;
-  const int pbeg = split * p.pages_per_split;
-  const int pend = min(pbeg + p.pages_per_split, npages);
-  const int ntiles = pend > pbeg ? (pend - pbeg + 7) / 8 : 0;
-  const int cap0 = (p.nq + 1) & ~1;
-  const int last_valid = L + p.gamma;
 
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) {
@@ -201,28 +136,87 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(drain, 1);
     fence_mbar_init();
   }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  // Nothing above reads or writes global memory, so it overlaps the tail of
+  // the previous kernel of the stream.
+  griddep_wait();
+
+  // Warps 1-9 request their chunks of the window queries first, so those
+  // loads are in flight together with the context-length load below.
+  constexpr int SN = 288;                      // threads of warps 1..9
+  constexpr int QPER = (NQP * 16 + SN - 1) / SN;
+  uint4 qreg[QPER];
+#pragma unroll
+  for (int u = 0; u < QPER; ++u) {
+    const int i = tid - 32 + u * SN, n = i >> 4, c = i & 15;
+    qreg[u] = make_uint4(0, 0, 0, 0);
+    if (warp >= 1 && warp <= 9 && i < NQP * 16 && n < p.nq) {
+      const int t = n / p.group, hl = n - t * p.group;
+      qreg[u] = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                               ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D)[c];
+    }
+  }
+  // Producer roles (warps 0, 10, 11).  TMA issue rate is per warp, so a
+  // tile's 32 boxes (8 pages x 2 column halves, of K and of V) are spread over
+  // three warps, in half-warps:
+  //   warp 0,  lanes 0-15:  K pages 0-5, arms the K slot's barrier;
+  //   warp 10, lanes 0-15:  V pages 0-5, arms the V slot's barrier;
+  //   warp 11, lanes 0-15:  K pages 6-7;  lanes 16-31: V pages 6-7.
+  // Lane j < np of a half-warp loads page pf + j (two 64-column boxes).
+  const int half = lane >> 4, hl = lane & 15;
+  const unsigned hmask = 0xFFFFu << (16 * half);
+  const bool producer = warp == 0 || warp >= 10;
+  const bool active = producer && (warp == 11 || half == 0);
+  const bool is_k = warp == 11 ? half == 0 : warp == 0;
+  const bool arms = warp != 11;
+  const int pf = warp == 11 ? 6 : 0, np = warp == 11 ? 2 : 6;
+  const int pbeg = split * p.pages_per_split;
+  const int32_t* bt_row = p.block_table + size_t(b) * p.max_pages;
+  // Block-table entries are prefetched four tiles ahead, one register per
+  // tile modulo 4, so a load is consumed four iterations after its issue.
+  // The loads do not wait for the context length: lane np of the half-warp
+  // loads the tile's first page, which stands in for pages past the end of
+  // the range (loaded again and masked by the softmax), and indices are
+  // clamped to the row.
+  auto table_entry = [&](int tt) {
+    if (hl > np) return 0;
+    const int page = pbeg + 8 * tt + (hl < np ? pf + hl : 0);
+    return __ldg(&bt_row[min(page, p.max_pages - 1)]);
+  };
+  int held[4] = {0, 0, 0, 0};
+  if (active) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) held[j] = table_entry(j);
+  }
+
+  int L = p.ctx_lens[b];
+  if (L < 0 || L + T > cap) {
+    if (tid == 0) set_error(p.err, kErrDeviceFault);
+    L = max(0, min(L, cap - T));
+  }
+  const int npages = (L + T + 15) / 16;
+  const int pend = min(pbeg + p.pages_per_split, npages);
+  const int ntiles = pend > pbeg ? (pend - pbeg + 7) / 8 : 0;
+  const int cap0 = (p.nq + 1) & ~1;
+  const int last_valid = L + p.gamma;
+
   __syncthreads();   // barriers initialised before anyone waits on them
   // Warps 0 and 10 start streaming K and V right away; warps 1-9 meanwhile
-  // allocate tensor memory and build the Q^T operand.
-  constexpr int SN = 288;                      // threads of warps 1..9
+  // build the Q^T operand.
   uint32_t tmem = 0;
   if (warp >= 1 && warp <= 9) {
     const int st = tid - 32;
-    if (warp == 1) {
-      tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
-      tmem_relinquish();
-    }
     // Q^T operand, K-major with the 128-byte swizzle: element (n, k) at
     // (k / 64) * NQP * 128 + n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16 + (k % 8) * 2.
-    for (int i = st; i < NQP * 16; i += SN) {
-      const int n = i >> 4, c = i & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (n < p.nq) {
-        const int t = n / p.group, hl = n - t * p.group;
-        v = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                           ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D)[c];
-      }
-      *reinterpret_cast<uint4*>(qs + (c >> 3) * (NQP * 128) + n * 128 + (((c & 7) ^ (n & 7)) << 4)) = v;
+#pragma unroll
+    for (int u = 0; u < QPER; ++u) {
+      const int i = st + u * SN, n = i >> 4, c = i & 15;
+      if (i < NQP * 16)
+        *reinterpret_cast<uint4*>(qs + (c >> 3) * (NQP * 128) + n * 128 + (((c & 7) ^ (n & 7)) << 4)) =
+            qreg[u];
     }
     for (int n = st; n < NQP; n += SN) {
       tlim[n] = n < p.nq ? min(n / p.group, p.gamma) : -1;
@@ -267,37 +261,20 @@ __global__ void __launch_bounds__(384, 1)
     tmem = *tmem_slot;
   }
   bool ok = true;
+  // A softmax group's final partial state for head dimension i: O^T row i
+  // (unnormalised), and column i's running maximum and row sum (i < NQC).
+  float o[NQC];
+  float Mg = kEmptyMax, Lg = 0.f;
+  const bool on_chip = p.cluster_merge || p.num_splits == 1;
 
   if (warp == 0 || warp >= 10) {
     // ------------------------------------------------------------ producers
-    // TMA issue rate is per warp, so a tile's 32 boxes (8 pages x 2 column
-    // halves, of K and of V) are spread over three warps, in half-warps:
-    //   warp 0,  lanes 0-15:  K pages 0-5, arms the K slot's barrier;
-    //   warp 10, lanes 0-15:  V pages 0-5, arms the V slot's barrier;
-    //   warp 11, lanes 0-15:  K pages 6-7;  lanes 16-31: V pages 6-7.
-    // Lane j < np of a half-warp loads page pf + j (two 64-column boxes).
-    const int half = lane >> 4, hl = lane & 15;
-    const unsigned hmask = 0xFFFFu << (16 * half);
-    const bool active = warp == 11 || half == 0;
-    const bool is_k = warp == 11 ? half == 0 : warp == 0;
-    const bool arms = warp != 11;
-    const int pf = warp == 11 ? 6 : 0, np = warp == 11 ? 2 : 6;
+    // (roles and the first block-table entries: above)
     const int depth = is_k ? KS : VS;
     const CUtensorMap* map = is_k ? &kmap : &vmap;
     const uint32_t ring = sbase + (is_k ? 0 : Cfg::kOffV);
-    const int32_t* bt_row = p.block_table + size_t(b) * p.max_pages;
-    // Block-table entries are prefetched four tiles ahead, one register per
-    // tile modulo 4, so a load is consumed four iterations after its issue.
-    auto table_entry = [&](int tt) {
-      int page = pbeg + 8 * tt + pf + hl;
-      if (page >= pend) page = pbeg + 8 * tt;         // loaded again, masked by the softmax
-      return (hl < np && tt < ntiles) ? __ldg(&bt_row[page]) : 0;
-    };
     int issued = 0;
     if (active) {
-      int held[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) held[j] = table_entry(j);
       for (int t0 = 0; t0 < ntiles && ok; t0 += 4) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -313,6 +290,8 @@ __global__ void __launch_bounds__(384, 1)
             break;
           }
           int phys = held[j];
+          const int first = __shfl_sync(hmask, phys, np, 16);
+          if (pbeg + 8 * t + pf + hl >= pend) phys = first;
           held[j] = table_entry(t + 4);
           if (hl < np && (phys < 0 || phys >= p.num_pages)) {
             set_error(p.err, kErrDeviceFault);
@@ -562,7 +541,6 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) colsum[(grp * 4 + q4) * NQC + n] = v;
     }
     // this thread's O^T row (head dimension i), unnormalised
-    float o[NQC];
 #pragma unroll
     for (int n = 0; n < NQC; ++n) o[n] = 0.f;
     if (mytiles > 0) {
@@ -576,7 +554,6 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait();
     }
     named_bar(1 + grp, 128);
-    float Mg = kEmptyMax, Lg = 0.f;                // column i's state (i < NQC)
     if (i < NQC) {
       const float* cs = colsum + grp * 4 * NQC;
       if (mytiles > 0) Lg = cs[i] + cs[NQC + i] + cs[2 * NQC + i] + cs[3 * NQC + i];
@@ -584,19 +561,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int n = 0; n < NQC; ++n)
         if (n == i) Mg = m[n];
     }
-    // Both groups past their last PV: every MMA has completed and every loaded
-    // tile was consumed, so the K ring is free for the staged states.
-    named_bar(3, 256);
-    if (p.cluster_merge || p.num_splits == 1) {
-      float* st = reinterpret_cast<float*>(smem) + grp * kTcStateFloats<NQC>;
-#pragma unroll
-      for (int n = 0; n < NQC; ++n)
-        if (n < p.nq) st[n * D + i] = o[n];
-      if (i < p.nq) {
-        st[NQC * D + i] = Mg;
-        st[NQC * D + NQC + i] = Lg;
-      }
-    } else {
+    if (!on_chip) {
       // partial 2 * split + grp of the unit's 2 * num_splits
       const size_t part = (size_t(unit) * p.num_splits + split) * 2 + grp;
 #pragma unroll
@@ -609,45 +574,75 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
 
+  // Every CTA of the cluster is past its last MMA and holds no load in flight,
+  // so its K ring is free from here on.
   tc_fence_before();
-  __syncthreads();
+  if (on_chip)
+    cluster_sync_all();
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
-  {
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-    auto out_row = [&](int n) {
-      const int t = n / p.group, hl = n - t * p.group;
-      return out + ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D;
-    };
-    if (p.cluster_merge || p.num_splits == 1) {
-      // The CTA's two group states merge in place into state 0 first (shared
-      // memory only), so the cluster merge reads one state per CTA.
-      constexpr int SF = kTcStateFloats<NQC>;
-      float* st0 = reinterpret_cast<float*>(smem);
-      const float* st1 = st0 + SF;
-      for (int e = tid; e < p.nq * D; e += Cfg::kThreads) {
-        const int n = e / D;
-        const float m0 = st0[NQC * D + n], m1 = st1[NQC * D + n];
-        const float M = fmaxf(m0, m1);
-        st0[e] = ex2(m0 - M) * st0[e] + ex2(m1 - M) * st1[e];
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+  auto out_row = [&](int n) {
+    const int t = n / p.group, hl2 = n - t * p.group;
+    return out + ((size_t(b) * T + t) * p.hq + g * p.group + hl2) * D;
+  };
+  if (on_chip) {
+    // Split-KV merge on chip (one split: a cluster of one CTA).  Row n of the
+    // output belongs to cluster rank n % S, which receives in its K ring, at
+    // slot n / S, the 2S partial states of the row (state 2 * rank + group of
+    // each sender, O[D] then m and l), pushed with distributed-shared-memory
+    // stores; one cluster barrier publishes them and each rank merges its rows
+    // from local shared memory (merge rule as in split_merge.cuh).  Nothing
+    // reads another CTA's shared memory, so no barrier precedes the exit.
+    constexpr int RS = D + 2;
+    static_assert(2 * (NQC + kMaxVerifyCluster) * RS * 4 <= KS * Cfg::kKV, "receive area");
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = p.num_splits, r = (int)cluster.block_rank();
+    const float* recv = reinterpret_cast<const float*>(smem);
+    if (warp >= 2 && warp <= 9) {
+      const int grp = (warp - 2) >> 2, i = 32 * (warp & 3) + lane;
+      const int q = 2 * r + grp;
+      int owner = 0, slot = 0;
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) {
+        if (n < p.nq)
+          st_cluster_f32(cluster_map(sbase + 4 * ((slot * 2 * S + q) * RS + i), owner), o[n]);
+        if (++owner == S) {
+          owner = 0;
+          ++slot;
+        }
       }
-      __syncthreads();   // every element read the maxima before they change
-      if (tid < p.nq) {
-        const float m0 = st0[NQC * D + tid], m1 = st1[NQC * D + tid];
-        const float M = fmaxf(m0, m1);
-        st0[NQC * D + NQC + tid] =
-            ex2(m0 - M) * st0[NQC * D + NQC + tid] + ex2(m1 - M) * st1[NQC * D + NQC + tid];
-        st0[NQC * D + tid] = M;
+      if (i < p.nq) {
+        const uint32_t dst = cluster_map(sbase + 4 * (((i / S) * 2 * S + q) * RS + D), i % S);
+        st_cluster_f32(dst, Mg);
+        st_cluster_f32(dst + 4, Lg);
       }
-      // (one split: a cluster of one CTA)
-      cluster_merge_rows<NQC>(st0, p.num_splits, p.nq, out_row);
-    } else {
-      SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
-      finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, 2 * p.num_splits, p.nq, out_row,
-                                           reinterpret_cast<float*>(smem), flag);
     }
+    cluster_sync_all();
+    const int nown = r < p.nq ? (p.nq - r + S - 1) / S : 0;
+    for (int e = tid; e < nown * D; e += Cfg::kThreads) {
+      const int k = e / D, d = e - k * D;
+      const float* st = recv + k * 2 * S * RS;
+      float M = kEmptyMax;
+#pragma unroll 8
+      for (int q = 0; q < 2 * S; ++q) M = fmaxf(M, st[q * RS + D]);
+      float Ls = 0.f, O = 0.f;
+#pragma unroll 8
+      for (int q = 0; q < 2 * S; ++q) {
+        const float f = ex2(st[q * RS + D] - M);
+        Ls += f * st[q * RS + D + 1];
+        O += f * st[q * RS + d];
+      }
+      out_row(r + k * S)[d] = __float2bfloat16_rn(Ls > 0.f ? O / Ls : 0.f);
+    }
+  } else {
+    SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
+    finish_splits<D, Cfg::kThreads, NQC>(ws, unit, p.num_splits, 2 * p.num_splits, p.nq, out_row,
+                                         reinterpret_cast<float*>(smem), flag);
   }
 }
 
