@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(384, 1)
     const int depth = is_k ? KS : VS;
     const CUtensorMap* map = is_k ? &kmap : &vmap;
     const uint32_t ring = sbase + (is_k ? 0 : Cfg::kOffV);
+    // The cache is streamed once per pass: its lines leave L2 first, so the
+    // scores, queries and block table stay there for the kernels after this.
+    const uint64_t stream_pol = l2_evict_first_policy();
     int issued = 0;
     if (active) {
       for (int t0 = 0; t0 < ntiles && ok; t0 += 4) {
@@ -304,8 +307,8 @@ __global__ void __launch_bounds__(384, 1)
           if (hl < np) {
             const int row = (phys * p.hkv + g) * 16;
             const uint32_t dst = ring + s * Cfg::kKV + (pf + hl) * 2048;
-            tma_load_2d(dst, map, 0, row, full);
-            tma_load_2d(dst + 16384, map, 64, row, full);
+            tma_load_2d_hint(dst, map, 0, row, full, stream_pol);
+            tma_load_2d_hint(dst + 16384, map, 64, row, full, stream_pol);
           }
           __syncwarp(hmask);
           issued = t + 1;
