@@ -15,8 +15,9 @@
 // groups with one 1-D bulk copy per K row and per V row (lanes 0-15 K, 16-31
 // V) into padded rows and runs the same warp core as the verify kernel with
 // the G query heads of the group as the tile's columns.  The CTAs' softmax
-// states meet in distributed shared memory: each CTA merges a slice of the
-// output elements and writes it, with no global scratch and no second pass.
+// states meet in distributed shared memory: each CTA pushes the slices of its
+// state to the CTAs that own them, then merges and writes the slice it owns,
+// with no global scratch and no second pass.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -43,6 +44,8 @@ constexpr size_t sparse_smem_layout_bytes() {
          + size_t(kAttnWarps) * SparseCfg<D>::kStages * 8          // mbarriers
          + size_t(SparseCfg<D>::kMaxRows) * 4                      // row table
          + size_t(NT) * 8 * (D + 2) * 4                            // CTA partial
+         + (size_t(NT) * 8 * D + kMaxSparseCluster) * 4              // received output slices
+         + size_t(kMaxSparseCluster) * NT * 8 * 2 * 4                // received m, l
          + 1024;
 }
 
@@ -58,6 +61,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   constexpr int QROW = 2 * D + 16;
   using Tile = PaddedTile<D>;
 
+  // First phase of the cluster barrier: this CTA has started (its shared
+  // memory may receive other CTAs' stores once every CTA has arrived).
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   griddep_begin();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -73,6 +79,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   float* pM = reinterpret_cast<float*>(rows + SparseCfg<D>::kMaxRows);   // [NPAD] CTA partial
   float* pL = pM + NPAD;                                                 // [NPAD]
   float* pO = pL + NPAD;                                                 // [NPAD][D]
+  float* rO = pO + NPAD * D;                     // [CL][per] output slices received
+  float* rM = rO + NPAD * D + kMaxSparseCluster; // [CL][NPAD] maxima received
+  float* rL = rM + kMaxSparseCluster * NPAD;     // [CL][NPAD] row sums received
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -216,14 +225,34 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   __syncthreads();
   cta_merge_to_smem<D, NT, W>(st, stage_area, SparseCfg<D>::kStageBytes, p.group, pM, pL, pO);
 
-  // Cluster merge: every CTA merges a slice of the G x D output elements,
-  // reading every CTA's state through distributed shared memory in one round
-  // trip: M = max_r m_r, O = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r.
-  cluster.sync();
+  // Cluster merge: CTA r owns the output elements [r * per, (r + 1) * per) of
+  // the G x D.  Every CTA pushes the slices of its state to their owners'
+  // receive areas with distributed-shared-memory stores (each thread the
+  // elements it merged above, threads n < G the row maxima and sums), one
+  // cluster barrier publishes them, and each owner merges locally:
+  // M = max_r m_r, O = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r.
+  // The receive areas are used by nothing else, so only the barrier phase
+  // begun at entry (every CTA has started) precedes the stores.
+  const int nel = p.group * D;
+  const int per = (nel + CL - 1) / CL;
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   {
-    constexpr int R = kMaxSparseCluster;   // remote loads are issued together, unrolled
-    const int nel = p.group * D;
-    const int per = (nel + CL - 1) / CL;
+    const uint32_t rO_s = smem_u32(rO), rM_s = smem_u32(rM), rL_s = smem_u32(rL);
+    for (int e = tid; e < nel; e += NTH) {
+      const int owner = e / per;
+      st_cluster_f32(cluster_map(rO_s + 4 * (rank * per + e - owner * per), owner), pO[e]);
+    }
+    if (tid < p.group) {
+      for (int r = 0; r < CL; ++r) {
+        st_cluster_f32(cluster_map(rM_s + 4 * (rank * NPAD + tid), r), pM[tid]);
+        st_cluster_f32(cluster_map(rL_s + 4 * (rank * NPAD + tid), r), pL[tid]);
+      }
+    }
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  {
+    constexpr int R = kMaxSparseCluster;
     const int e0 = rank * per, e1 = min(nel, e0 + per);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     for (int e = e0 + tid; e < e1; e += NTH) {
@@ -234,9 +263,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
         mr[r] = -INFINITY;
         lr[r] = v[r] = 0.f;
         if (r < CL) {
-          mr[r] = cluster.map_shared_rank(pM, r)[n];
-          lr[r] = cluster.map_shared_rank(pL, r)[n];
-          v[r] = cluster.map_shared_rank(pO, r)[e];
+          mr[r] = rM[r * NPAD + n];
+          lr[r] = rL[r * NPAD + n];
+          v[r] = rO[r * per + e - e0];
         }
       }
       float M = -INFINITY;
@@ -253,7 +282,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
           __float2bfloat16_rn(L > 0.f ? a / L : 0.f);
     }
   }
-  cluster.sync();   // no CTA leaves while another may still read its shared memory
 }
 
 template <int D, int NT>

@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(VerifyCfg<D, NT>::W * 32, 1)
       const uint32_t bar = bar0 + s * 8;
       const uint32_t dst = stage0 + s * STAGE;
       mbar_arrive_expect_tx(bar, STAGE);
+      // read once per pass: the tiles leave L2 first, so the scores, queries
+      // and block table stay there for the kernels after this
+      const uint64_t pol = l2_evict_first_policy();
 #pragma unroll
       for (int pg = 0; pg < P; ++pg) {
         int ph = phys[pg];
@@ -133,8 +136,8 @@ __global__ void __launch_bounds__(VerifyCfg<D, NT>::W * 32, 1)
         const int row = (ph * p.hkv + g) * 16;
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_2d(dst + pg * TILE + h * 2048, &kmap, h * 64, row, bar);
-          tma_load_2d(dst + (P + pg) * TILE + h * 2048, &vmap, h * 64, row, bar);
+          tma_load_2d_hint(dst + pg * TILE + h * 2048, &kmap, h * 64, row, bar, pol);
+          tma_load_2d_hint(dst + (P + pg) * TILE + h * 2048, &vmap, h * 64, row, bar, pol);
         }
       }
     }
