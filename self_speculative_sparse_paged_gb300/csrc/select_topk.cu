@@ -40,8 +40,6 @@
 // written to every KV head's row.
 #include <cooperative_groups.h>
 
-#include <algorithm>
-
 #include "kernels.h"
 #include "vegas_common.cuh"
 
@@ -468,14 +466,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   cluster_wait();     // no CTA leaves while another may still read its shared memory
 }
 
-// At least half of an SM's shared memory, so no two CTAs share an SM: a CTA
-// that shares one (which the scheduler does when a kernel holding most SMs,
-// such as the verify pass, leaves fewer free SMs per GPC than the cluster has
-// CTAs) slows every level barrier of its cluster.
-constexpr size_t kSelSmemFloor = 116 * 1024;
-size_t select_smem_bytes(int chunk) {
-  return std::max(size_t(kLevelWords + chunk) * 4, kSelSmemFloor);
-}
+size_t select_smem_bytes(int chunk) { return size_t(kLevelWords + chunk) * 4; }
 
 template <int P, bool SHARED>
 static cudaError_t launch_select_p(const SelectParams& p, int cluster, int batch,
