@@ -95,8 +95,8 @@ typedef struct {
  * rows 0 and gamma under this library's reading).  capture_row_a ==
  * capture_row_b captures one row once.  Entries at i >= L_b are not written.
  *
- *   q:   device bf16 [batch][gamma + 1][num_q_heads][head_dim]
- *   out: device bf16, same shape as q
+ *   q:   device bf16 [batch][gamma + 1][num_q_heads][head_dim], 16-byte aligned
+ *   out: device bf16, same shape as q, 16-byte aligned
  *   ctx_lens: device int32 [batch]; needs L_b + gamma + 1 <= 16 * max_pages_per_seq
  *   score_stride >= max_b L_b when scores != NULL
  * Supported: head_dim in {64, 128}; (gamma + 1) * G <= 64 with G = Hq / Hkv;

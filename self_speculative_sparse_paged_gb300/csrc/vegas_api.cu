@@ -343,7 +343,8 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   if (batch < 0) return fail(VEGAS_ERR_INVALID_ARG, "batch %d", batch);
   if (gamma < 0 || gamma > 15) return fail(VEGAS_ERR_UNSUPPORTED, "gamma %d (0..15)", gamma);
   if (!q || !out || !ctx_lens) return fail(VEGAS_ERR_INVALID_ARG, "NULL q, out or ctx_lens");
-  if (!aligned16(q)) return fail(VEGAS_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!aligned16(q) || !aligned16(out))
+    return fail(VEGAS_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
   if (!std::isfinite(softmax_scale)) return fail(VEGAS_ERR_INVALID_ARG, "softmax_scale not finite");
   const int G = kv->num_q_heads / kv->num_kv_heads;
   const int nq = (gamma + 1) * G;

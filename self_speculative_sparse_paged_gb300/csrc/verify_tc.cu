@@ -599,10 +599,12 @@ __global__ void __launch_bounds__(384, 1)
     // slot n / S, the 2S partial states of the row (state 2 * rank + group of
     // each sender, O[D] then m and l), pushed with distributed-shared-memory
     // stores; one cluster barrier publishes them and each rank merges its rows
-    // from local shared memory (merge rule as in split_merge.cuh).  Nothing
-    // reads another CTA's shared memory, so no barrier precedes the exit.
-    constexpr int RS = D + 2;
+    // from local shared memory: O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q
+    // with M = max_q m_q.  Nothing reads another CTA's shared memory, so no
+    // barrier precedes the exit.
+    constexpr int RS = D + 4;   // one received state: O[D], m, l, padding to 16 bytes
     static_assert(2 * (NQC + kMaxVerifyCluster) * RS * 4 <= KS * Cfg::kKV, "receive area");
+    static_assert(2 * kMaxVerifyCluster <= 32, "one lane per state in the weight pass");
     cg::cluster_group cluster = cg::this_cluster();
     const int S = p.num_splits, r = (int)cluster.block_rank();
     const float* recv = reinterpret_cast<const float*>(smem);
@@ -627,20 +629,45 @@ __global__ void __launch_bounds__(384, 1)
     }
     cluster_sync_all();
     const int nown = r < p.nq ? (p.nq - r + S - 1) / S : 0;
-    for (int e = tid; e < nown * D; e += Cfg::kThreads) {
-      const int k = e / D, d = e - k * D;
+    // Weights 2^(m_q - M) / sum_q' 2^(m_q' - M) l_q' of the 2S states of each
+    // owned row (one warp per row, lane q), into the free V ring ...
+    float* wts = reinterpret_cast<float*>(smem + Cfg::kOffV);   // [nown][2S]
+    for (int k = warp; k < nown; k += Cfg::kThreads / 32) {
       const float* st = recv + k * 2 * S * RS;
-      float M = kEmptyMax;
-#pragma unroll 8
-      for (int q = 0; q < 2 * S; ++q) M = fmaxf(M, st[q * RS + D]);
-      float Ls = 0.f, O = 0.f;
+      const bool has = lane < 2 * S;
+      const float m = has ? st[lane * RS + D] : kEmptyMax;
+      const float l = has ? st[lane * RS + D + 1] : 0.f;
+      float M = m;
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+      const float f = has ? ex2(m - M) : 0.f;
+      float Lsum = f * l;
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o2);
+      if (has) wts[k * 2 * S + lane] = Lsum > 0.f ? f / Lsum : 0.f;
+    }
+    __syncthreads();
+    // ... then four output elements per thread: sum_q w_q O_q[d .. d + 3]
+    for (int e = tid; e < nown * (D / 4); e += Cfg::kThreads) {
+      const int k = e / (D / 4), d = 4 * (e - k * (D / 4));
+      const float* st = recv + k * 2 * S * RS + d;
+      const float* wk = wts + k * 2 * S;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
       for (int q = 0; q < 2 * S; ++q) {
-        const float f = ex2(st[q * RS + D] - M);
-        Ls += f * st[q * RS + D + 1];
-        O += f * st[q * RS + d];
+        const float4 v = *reinterpret_cast<const float4*>(st + q * RS);
+        const float wq = wk[q];
+        acc.x += wq * v.x;
+        acc.y += wq * v.y;
+        acc.z += wq * v.z;
+        acc.w += wq * v.w;
       }
-      out_row(r + k * S)[d] = __float2bfloat16_rn(Ls > 0.f ? O / Ls : 0.f);
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out_row(r + k * S) + d) = pk;
     }
   } else {
     SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};

@@ -98,6 +98,12 @@ def test_host_validation_of_the_variant_entry_points(vg):
         vg.vegas_verify_attn_raw_logits(kv, 16, 16, 16, 64, 16, 1, 4, 1 << 7, 0.125, None, 0,
                                         stream=0)
     assert ei.value.status == 1
+    # q and out must be 16-byte aligned (the kernels store output rows in vectors)
+    kv16 = vg.PagedKV(16, 16, 16, 4, 16, 8, 2, 64, 4)
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_capture(kv16, 16, 18, None, 0, 16, 1, 4, 0, 4, 0.125, None, 0,
+                                     stream=0)
+    assert ei.value.status == 1 and "aligned" in ei.value.detail
     # aggregate: query heads must be a multiple of the KV heads
     with pytest.raises(vg.VegasError) as ei:
         vg.vegas_aggregate_raw_logits(16, 64, 16, 1, 2, 6, 4, 64, 16, 64, stream=0)
