@@ -55,14 +55,15 @@ def read_peaks():
 
 
 # DRAM traffic of one verify launch (dram__bytes_read.sum + dram__bytes_write.sum)
-# on this workload, from the ncu launch list in
-# profiles/launch_list_qwen3_8b_b1_32k.md; reported only while the kernel
-# sources still hash to the digest they had when the counters were taken.
+# on this workload, from a one-pass ncu capture of the verify launches of
+# `python bench.py --steps 8 --warmup 3 --no-cpu-baseline`; reported only while
+# the kernel sources still hash to the digest they had when the counters were
+# taken.
 VERIFY_TRAFFIC = {
-    "bytes": 134_870_000,
+    "bytes": 134_800_000,
     "sources": ["verify_tc.cu", "split_merge.cuh", "attn_core.cuh", "vegas_common.cuh",
                 "kernels.h"],
-    "sha256": "471f5508d7ff301cb469f27bde66f8db4a6f4bd69b701f725753c1076d811387",
+    "sha256": "1f65197358ad7fb2ad22940dd40f7d1ca0f86fde912b9f377bc2825212467b00",
 }
 
 
