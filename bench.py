@@ -754,7 +754,16 @@ def main():
                             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                             "traffic": verify_traffic_bytes(),
-                            "bytes_per_launch": nbytes["verify"]}
+                            "bytes_per_launch": nbytes["verify"],
+                            "duration_us": round(v_us, 3),
+                            "duration_source": "stage events around the verify launch (the "
+                                               "events cut its programmatic-launch overlap)"}
+        b2b = variants.get("verify_capture2_us")
+        if b2b:
+            a2 = nbytes["verify"] / (b2b * 1e-6) / 1e9
+            # context: the same kernel timed as a graph of 100 launches back to back
+            line["roofline"]["back_to_back"] = {"duration_us": b2b, "achieved": round(a2, 1),
+                                                "frac": round(a2 / peak, 4)}
     # the "next" rows, measured the same way on the same workload: collect-all
     # capture, one T shared by all heads, the query-agnostic window selector
     line["variants"] = variants
