@@ -679,6 +679,25 @@ def time_oracle(w, nbytes, budget_s, min_steps=1, max_steps=None):
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
+def roofline_entry(bytes_per_launch, duration_us, peak, peak_kind, back_to_back_us=None):
+    """The bench line's roofline object for the verify kernel: algorithmic bytes
+    per launch over its stage-event duration against the HBM peak, the ncu
+    traffic while the sources match, and (context) the same bytes over the
+    per-launch time of a graph of launches back to back."""
+    achieved = bytes_per_launch / (duration_us * 1e-6) / 1e9
+    out = {"kernel": "verify_tc_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+           "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+           "peak_kind": peak_kind, "traffic": verify_traffic_bytes(),
+           "bytes_per_launch": bytes_per_launch, "duration_us": round(duration_us, 3),
+           "duration_source": "stage events around the verify launch (the events cut its "
+                              "programmatic-launch overlap)"}
+    if back_to_back_us:
+        a2 = bytes_per_launch / (back_to_back_us * 1e-6) / 1e9
+        out["back_to_back"] = {"duration_us": back_to_back_us, "achieved": round(a2, 1),
+                               "frac": round(a2 / peak, 4)}
+    return out
+
+
 def base_config(w, lens, kps):
     return {"workload": w.name, "description": w.description, "batch": w.batch,
             "ctx_len": int(lens.max()), "gamma": w.gamma, "k": int(kps.max()),
@@ -749,21 +768,8 @@ def main():
         line["stages"]["verify_plain_us"] = round(verify_plain_us, 3)
         line["capture_plus_select_overhead"] = round(
             (v_us + stages["select_us"]) / verify_plain_us - 1.0, 4)
-        achieved = nbytes["verify"] / (v_us * 1e-6) / 1e9
-        line["roofline"] = {"kernel": "verify_tc_kernel", "bound": "hbm",
-                            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                            "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                            "traffic": verify_traffic_bytes(),
-                            "bytes_per_launch": nbytes["verify"],
-                            "duration_us": round(v_us, 3),
-                            "duration_source": "stage events around the verify launch (the "
-                                               "events cut its programmatic-launch overlap)"}
-        b2b = variants.get("verify_capture2_us")
-        if b2b:
-            a2 = nbytes["verify"] / (b2b * 1e-6) / 1e9
-            # context: the same kernel timed as a graph of 100 launches back to back
-            line["roofline"]["back_to_back"] = {"duration_us": b2b, "achieved": round(a2, 1),
-                                                "frac": round(a2 / peak, 4)}
+        line["roofline"] = roofline_entry(nbytes["verify"], v_us, peak, peak_kind,
+                                          variants.get("verify_capture2_us"))
     # the "next" rows, measured the same way on the same workload: collect-all
     # capture, one T shared by all heads, the query-agnostic window selector
     line["variants"] = variants

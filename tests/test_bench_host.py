@@ -1,0 +1,42 @@
+"""Host-side pieces of bench.py's JSON line, checked without a GPU."""
+import math
+
+import bench
+from workload import configs, gen
+
+
+def test_roofline_entry_fields_and_arithmetic():
+    r = bench.roofline_entry(135_368_704, 34.88, 6795.5, "measured", back_to_back_us=29.56)
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in r
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert math.isclose(r["achieved"], 135_368_704 / 34.88e-6 / 1e9, rel_tol=1e-4)
+    assert math.isclose(r["frac"], r["achieved"] / 6795.5, rel_tol=1e-3)
+    b = r["back_to_back"]
+    assert b["achieved"] > r["achieved"] and math.isclose(b["frac"], b["achieved"] / 6795.5,
+                                                          rel_tol=1e-3)
+    assert "back_to_back" not in bench.roofline_entry(1e8, 10.0, 6795.5, "measured")
+
+
+def test_traffic_is_null_or_the_recorded_capture():
+    """Reported only while the kernel sources hash to the digest of the capture,
+    and then close to the algorithmic bytes (no wasted re-reads)."""
+    t = bench.verify_traffic_bytes()
+    assert t is None or t == bench.VERIFY_TRAFFIC["bytes"]
+    w = configs.QWEN3_8B_B1_32K
+    lens = gen.ctx_lens(w)
+    alg = bench.algorithmic_bytes(w, lens, gen.k_per_seq(w, lens))["verify"]
+    assert abs(bench.VERIFY_TRAFFIC["bytes"] / alg - 1.0) < 0.02
+
+
+def test_algorithmic_bytes_of_the_bench_workload():
+    """K and V of every prefix and window position, once, plus queries, outputs and
+    scores: the per-launch figure the roofline divides by."""
+    w = configs.QWEN3_8B_B1_32K
+    lens = gen.ctx_lens(w)
+    kps = gen.k_per_seq(w, lens)
+    nb = bench.algorithmic_bytes(w, lens, kps)
+    L = int(lens[0])
+    kv = 2 * w.hkv * (L + w.gamma + 1) * w.head_dim * 2
+    assert kv <= nb["verify"] <= kv + 2 * 1024 * 1024
+    assert nb["total"] > nb["verify"]
