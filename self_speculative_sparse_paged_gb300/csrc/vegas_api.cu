@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -35,28 +36,34 @@ vegas_status_t cuda_fail(cudaError_t e, const char* where) {
 }
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int* g_err_ptr[kMaxDevices] = {};
-int g_sms[kMaxDevices] = {};
+std::mutex g_mu;   // serialises the first lookup per device only
+std::atomic<int*> g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};   // written before g_err_ptr[dev] is published
 
-// Device address of the error word and SM count of the current device.
+// Device address of the error word and SM count of the current device (looked
+// up once per device; later calls take no lock).
 vegas_status_t device_info(int** err, int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(VEGAS_ERR_UNSUPPORTED, "device ordinal %d", dev);
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_err_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_error_word);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    g_sms[dev] = n;
-    g_err_ptr[dev] = static_cast<int*>(p);
+  int* ep = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (!ep) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ep = g_err_ptr[dev].load(std::memory_order_relaxed);
+    if (!ep) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_error_word);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+      int n = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+      g_sms[dev] = n;
+      ep = static_cast<int*>(p);
+      g_err_ptr[dev].store(ep, std::memory_order_release);
+    }
   }
-  if (err) *err = g_err_ptr[dev];
+  if (err) *err = ep;
   if (sms) *sms = g_sms[dev];
   return VEGAS_OK;
 }
