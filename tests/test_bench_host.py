@@ -40,3 +40,13 @@ def test_algorithmic_bytes_of_the_bench_workload():
     kv = 2 * w.hkv * (L + w.gamma + 1) * w.head_dim * 2
     assert kv <= nb["verify"] <= kv + 2 * 1024 * 1024
     assert nb["total"] > nb["verify"]
+
+
+def test_cpu_baseline_fields_on_the_tiny_workload():
+    """The cpu_baseline object: the oracle timed on host cores, with its sample stated."""
+    w = configs.TINY
+    lens = gen.ctx_lens(w)
+    nb = bench.algorithmic_bytes(w, lens, gen.k_per_seq(w, lens))
+    r = bench.time_oracle(w, nb, budget_s=0.5, max_steps=2)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["cores"] >= 1
+    assert r["value"] > 0 and r["steps"] == 2 and "KV heads" in r["sample"]
