@@ -239,6 +239,22 @@ vegas_status_t vegas_sparse_decode_attn(
     void* stream);
 
 /* ------------------------------------------------------------------------
+ * Failure-detection check (the paper has no counterpart).
+ *
+ * Every wait of these kernels on an on-chip barrier (a TMA tile landing, an
+ * MMA completing, a peer CTA's partial state) gives up after a time limit:
+ * the kernel then records VEGAS_ERR_DEVICE_TIMEOUT in the device error word,
+ * drains what it has in flight and returns, so a lost arrival cannot hang the
+ * GPU.  This call shows that protocol end to end: it launches one CTA that
+ * waits, with limit_us microseconds as its limit (1 .. 1000000), on a barrier
+ * nothing ever arrives on (with nothing else in flight), records the timeout
+ * and returns.  The next vegas_read_device_status() then returns
+ * VEGAS_ERR_DEVICE_TIMEOUT and clears the word.  If outcome is not NULL
+ * (device int32), it receives 0 when the wait ran out (1 if it completed).
+ * ---------------------------------------------------------------------- */
+vegas_status_t vegas_check_bounded_wait(int limit_us, int32_t* outcome, void* stream);
+
+/* ------------------------------------------------------------------------
  * Status.
  * ---------------------------------------------------------------------- */
 /* Synchronises `stream`, returns the current device's error word as a status

@@ -199,22 +199,45 @@ def select_topk_batch(scores: np.ndarray, ctx_lens: np.ndarray, k_per_seq: np.nd
     return out
 
 
+def summed_head_scores(scores: np.ndarray, L: int, b: int) -> np.ndarray:
+    """s[i] = sum over the KV heads g of scores[b][g][i], i < L, in fp64.
+
+    Each scores[b][g] already sums its group's query heads (capture_scores), so
+    this is the §2.A triple sum with H = every query head of the layer."""
+    return np.asarray(scores[b, :, :L], dtype=np.float64).sum(axis=0)
+
+
+def select_topk_shared_batch(scores: np.ndarray, ctx_lens: np.ndarray,
+                             k_per_seq: np.ndarray, k_max: int) -> np.ndarray:
+    """§2.A with H = every query head of the layer: one T per sequence, the k_b
+    positions of largest summed score sum_g s[b][g][i] (fp64), written to the
+    rows of every KV head.  [B][Hkv][k_max] int32, -1 padded."""
+    B, Hkv = scores.shape[0], scores.shape[1]
+    out = np.full((B, Hkv, k_max), -1, dtype=np.int32)
+    for b in range(B):
+        L, k = int(ctx_lens[b]), int(k_per_seq[b])
+        T = select_topk(summed_head_scores(scores, L, b), k)
+        for g in range(Hkv):
+            out[b, g, :k] = T
+    return out
+
+
 def summed_head_scores_f32(scores_f32: np.ndarray, L: int, b: int) -> np.ndarray:
-    """s[i] = sum over the KV heads g of scores[b][g][i], i < L, added in fp32 in
-    head order g = 0, 1, ... (the precision and order the selection decision is
-    taken in on both sides)."""
+    """The shared-T library call's stated key: sum over the KV heads of
+    scores[b][g][i], added in fp32 in head order g = 0, 1, ...  Not the method's
+    definition (that is summed_head_scores, fp64); it lets a test feed the
+    library and this oracle the same fp32 keys and demand identical indices."""
     s = np.array(scores_f32[b, 0, :L], dtype=np.float32)
     for g in range(1, scores_f32.shape[1]):
         s = (s + np.asarray(scores_f32[b, g, :L], dtype=np.float32)).astype(np.float32)
     return s
 
 
-def select_topk_shared_batch(scores_f32: np.ndarray, ctx_lens: np.ndarray,
-                             k_per_seq: np.ndarray, k_max: int) -> np.ndarray:
-    """§2.A with H = every query head of the layer: one T per sequence, the k_b
-    positions of largest summed score sum_g s[b][g][i] (which equals the triple
-    sum over all heads, since each s[b][g] already sums its group's heads),
-    written to the rows of every KV head.  [B][Hkv][k_max] int32, -1 padded."""
+def select_topk_shared_batch_f32(scores_f32: np.ndarray, ctx_lens: np.ndarray,
+                                 k_per_seq: np.ndarray, k_max: int) -> np.ndarray:
+    """select_topk_shared_batch on the fp32 head-order keys of
+    summed_head_scores_f32 (the library call's stated key, for the bit-exact
+    identical-keys comparison)."""
     B, Hkv = scores_f32.shape[0], scores_f32.shape[1]
     out = np.full((B, Hkv, k_max), -1, dtype=np.int32)
     for b in range(B):

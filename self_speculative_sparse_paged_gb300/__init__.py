@@ -21,7 +21,7 @@ __all__ = [
     "VegasError", "PagedKV", "paged_kv", "lib", "library_path",
     "vegas_verify_workspace_size", "vegas_verify_attn_capture", "vegas_select_topk",
     "vegas_sparse_decode_attn", "vegas_synth_paged_kv", "vegas_verify_attn_capture_noalloc",
-    "vegas_verify_noalloc_max_scratch_bytes",
+    "vegas_verify_noalloc_max_scratch_bytes", "vegas_check_bounded_wait",
     "vegas_read_device_status", "vegas_status_string", "vegas_last_error_detail",
     "vegas_abi_version",
 ]
@@ -112,6 +112,7 @@ _sparse = _sig("vegas_sparse_decode_attn", _i32,
 _synth = _sig("vegas_synth_paged_kv", _i32,
               [_c_void_p, _i32, _u64, _i32, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p,
                _c_void_p, _u64, _i32, _c_void_p, _c_void_p])
+_wait_check = _sig("vegas_check_bounded_wait", _i32, [_i32, _c_void_p, _c_void_p])
 _read_status = _sig("vegas_read_device_status", _i32, [_c_void_p])
 _status_string = _sig("vegas_status_string", ctypes.c_char_p, [_i32])
 _detail = _sig("vegas_last_error_detail", ctypes.c_char_p, [])
@@ -237,6 +238,11 @@ def vegas_synth_paged_kv(cache, which: int, seed: int, layer: int, owner, num_pa
     _check(_synth(_ptr(cache), which, seed, layer, _ptr(owner), num_pages, num_kv_heads,
                   head_dim, max_pages_per_seq, _ptr(ctx_lens), _ptr(positions), heavy_threshold,
                   heavy_last, _ptr(unit_dir), _stream(stream)))
+
+
+def vegas_check_bounded_wait(limit_us: int, outcome=None, stream=None) -> None:
+    """Launches the failure-detection check: a wait that runs out after limit_us."""
+    _check(_wait_check(limit_us, _ptr(outcome), _stream(stream)))
 
 
 def vegas_read_device_status(stream=None) -> None:

@@ -2,11 +2,13 @@
 
 nvcc compiles each translation unit for sm_103a in parallel; the verify kernel
 source is compiled once per (head_dim, capture) pair so its 28 instantiations
-spread over four units.  Objects are rebuilt only when a source or header is
-newer than the library.
+spread over four units.  The library is rebuilt unless the digest stored
+beside it matches the current sources, headers, flags and this script (a copied
+or stale binary is never trusted on its timestamp).
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -19,6 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libvegas.so")
+DIGEST = os.path.join(BUILD, "libvegas.sha256")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -32,6 +35,7 @@ UNITS = [
     ("select_topk.cu", "select_topk.o", []),
     ("select_window.cu", "select_window.o", []),
     ("raw_aggregate.cu", "raw_aggregate.o", []),
+    ("wait_check.cu", "wait_check.o", []),
     ("sparse_decode.cu", "sparse_decode.o", []),
     ("verify_attn.cu", "verify_d128_c1.o", ["-DVEGAS_D=128", "-DVEGAS_CAP=1"]),
     ("verify_attn.cu", "verify_d128_c0.o", ["-DVEGAS_D=128", "-DVEGAS_CAP=0"]),
@@ -47,15 +51,26 @@ def nvcc() -> str:
     return cand
 
 
-def _sources_mtime() -> float:
-    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    paths += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+def sources_digest() -> str:
+    """sha256 over every source and header (name and bytes), the units and
+    flags, and this script."""
+    h = hashlib.sha256()
+    paths = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
+    paths += sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE))
     paths.append(os.path.abspath(__file__))
-    return max(os.path.getmtime(p) for p in paths)
+    for p in paths:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(repr((FLAGS, UNITS)).encode())
+    return h.hexdigest()
 
 
 def up_to_date() -> bool:
-    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _sources_mtime()
+    if not (os.path.exists(LIB) and os.path.exists(DIGEST)):
+        return False
+    with open(DIGEST) as f:
+        return f.read().strip() == sources_digest()
 
 
 def build(verbose: bool = False, jobs: int | None = None) -> str:
@@ -63,6 +78,8 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     if up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    if os.path.exists(DIGEST):
+        os.remove(DIGEST)
     cc = nvcc()
 
     def compile_unit(unit):
@@ -84,6 +101,8 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(DIGEST, "w") as f:
+        f.write(sources_digest() + "\n")
     return LIB
 
 

@@ -7,6 +7,8 @@
 
 #include <atomic>
 
+#include "../../include/vegas.h"
+
 namespace vegas {
 
 constexpr int kAttnWarps = 8;          // warps per attention CTA
@@ -105,6 +107,17 @@ inline cudaError_t once_per_device(std::atomic<uint32_t>& done, F&& f) {
 // Records `msg` as this host thread's vegas_last_error_detail(); returns status.
 int record_failure(int status, const char* msg);
 
+// Supplies a library-owned verify workspace (address and size) on the current device.
+using ScratchFn = vegas_status_t (*)(void** workspace, size_t* bytes);
+// vegas_verify_attn_capture; when `scratch` is given and the shape needs a
+// workspace, it is asked for one only after every argument has been checked,
+// and the workspace's counters are cleared on the stream before the launch.
+vegas_status_t verify_two_rows(const vegas_paged_kv_t* kv, const void* q, void* out,
+                               float* scores, int score_stride, const int32_t* ctx_lens,
+                               int batch, int gamma, int capture_row_a, int capture_row_b,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               void* stream, ScratchFn scratch);
+
 // Shared-memory bytes and launch of each kernel; return cudaError_t.
 
 // Largest 8-row query tile count per head_dim (d=128: 48 rows, d=64: 64 rows).
@@ -133,6 +146,11 @@ cudaError_t launch_raw_aggregate(const RawAggParams& p, int batch, int max_len,
 int select_max_chunk();
 int select_chunk_quantum();   // a CTA's chunk is a multiple of this
 cudaError_t launch_select(const SelectParams& p, int cluster, int batch, cudaStream_t stream);
+
+// One CTA waits on an mbarrier nothing arrives on, bounded by limit_ns; on
+// running out it records kErrDeviceTimeout in *err and writes 0 to *outcome.
+cudaError_t launch_bounded_wait_check(unsigned long long limit_ns, int* err, int* outcome,
+                                      cudaStream_t stream);
 
 cudaError_t launch_synth_kv(void* cache, int which, uint64_t seed, int layer, const int32_t* owner,
                             int num_pages, int hkv, int head_dim, int max_pages,

@@ -262,13 +262,18 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
                            int score_stride, const int32_t* ctx_lens, int batch, int gamma,
                            uint32_t row_mask, float softmax_scale, void* workspace,
                            size_t workspace_bytes, void* stream, float* raw = nullptr,
-                           int raw_stride = 0);
+                           int raw_stride = 0, vegas::ScratchFn scratch = nullptr);
 }  // namespace
 
-VEGAS_API vegas_status_t vegas_verify_attn_capture(
-    const vegas_paged_kv_t* kv, const void* q, void* out, float* scores, int score_stride,
-    const int32_t* ctx_lens, int batch, int gamma, int capture_row_a, int capture_row_b,
-    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+namespace vegas {
+// vegas_verify_attn_capture; with `scratch`, the workspace comes from it once
+// every argument has been checked, and its counters are cleared on the stream
+// just before the launch.
+vegas_status_t verify_two_rows(const vegas_paged_kv_t* kv, const void* q, void* out,
+                               float* scores, int score_stride, const int32_t* ctx_lens,
+                               int batch, int gamma, int capture_row_a, int capture_row_b,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               void* stream, ScratchFn scratch) {
   uint32_t mask = 0;
   if (scores) {
     if (gamma < 0 || gamma > 15) return fail(VEGAS_ERR_UNSUPPORTED, "gamma %d (0..15)", gamma);
@@ -278,7 +283,17 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture(
     mask = (1u << capture_row_a) | (1u << capture_row_b);
   }
   return verify_impl(kv, q, out, scores, score_stride, ctx_lens, batch, gamma, mask,
-                     softmax_scale, workspace, workspace_bytes, stream);
+                     softmax_scale, workspace, workspace_bytes, stream, nullptr, 0, scratch);
+}
+}  // namespace vegas
+
+VEGAS_API vegas_status_t vegas_verify_attn_capture(
+    const vegas_paged_kv_t* kv, const void* q, void* out, float* scores, int score_stride,
+    const int32_t* ctx_lens, int batch, int gamma, int capture_row_a, int capture_row_b,
+    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return vegas::verify_two_rows(kv, q, out, scores, score_stride, ctx_lens, batch, gamma,
+                                capture_row_a, capture_row_b, softmax_scale, workspace,
+                                workspace_bytes, stream, nullptr);
 }
 
 VEGAS_API vegas_status_t vegas_verify_attn_raw_logits(
@@ -344,7 +359,8 @@ namespace {
 vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out, float* scores,
                            int score_stride, const int32_t* ctx_lens, int batch, int gamma,
                            uint32_t row_mask, float softmax_scale, void* workspace,
-                           size_t workspace_bytes, void* stream, float* raw, int raw_stride) {
+                           size_t workspace_bytes, void* stream, float* raw, int raw_stride,
+                           vegas::ScratchFn scratch) {
   vegas_status_t st = check_kv(kv);
   if (st != VEGAS_OK) return st;
   if (batch < 0) return fail(VEGAS_ERR_INVALID_ARG, "batch %d", batch);
@@ -367,7 +383,9 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   int sms = 0;
   if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
   const VerifyPlan pl = plan_verify(kv, batch, gamma, sms, scores != nullptr, true);
-  if (pl.splits > 1 && !pl.cluster) {
+  const bool needs_ws = pl.splits > 1 && !pl.cluster;
+  if (needs_ws && scratch && (st = scratch(&workspace, &workspace_bytes)) != VEGAS_OK) return st;
+  if (needs_ws) {
     if (!workspace || workspace_bytes < pl.bytes)
       return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "verify workspace %zu < %zu bytes",
                   workspace_bytes, pl.bytes);
@@ -405,6 +423,12 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   p.part_ml = ws ? reinterpret_cast<float*>(ws + pl.ml_off) : nullptr;
   p.part_o = ws ? reinterpret_cast<float*>(ws + pl.o_off) : nullptr;
   p.err = err;
+  if (needs_ws && scratch) {
+    // shared scratch: its per-unit counters may hold anything from an earlier call
+    cudaError_t e = cudaMemsetAsync(p.tickets, 0, size_t(batch) * kv->num_kv_heads * sizeof(int),
+                                    static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
+  }
   cudaError_t e =
       pl.tc ? vegas::launch_verify_tc(km, vm, p, pl.ncols, scores != nullptr, batch,
                                       static_cast<cudaStream_t>(stream))
@@ -583,6 +607,21 @@ VEGAS_API vegas_status_t vegas_synth_paged_kv(void* cache, int which, uint64_t s
                                          heavy_threshold, heavy_last, unit_dir,
                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "synth launch");
+  return VEGAS_OK;
+}
+
+// =========================================================================
+// Failure-detection check
+// =========================================================================
+VEGAS_API vegas_status_t vegas_check_bounded_wait(int limit_us, int* outcome, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(VEGAS_ERR_INVALID_ARG, "limit_us %d outside [1, 1000000]", limit_us);
+  int* err = nullptr;
+  vegas_status_t st = device_info(&err, nullptr);
+  if (st != VEGAS_OK) return st;
+  cudaError_t e = vegas::launch_bounded_wait_check(1000ull * (unsigned long long)limit_us, err,
+                                                   outcome, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait check launch");
   return VEGAS_OK;
 }
 

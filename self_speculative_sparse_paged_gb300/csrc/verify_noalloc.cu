@@ -14,9 +14,10 @@
 // that device current) on the first call there.  That first call on a device
 // should therefore come before any stream capture.
 //
-// All calls share the one array: the kernel's per-unit counters are cleared
-// on the stream at the start of every call, and calls whose work overlaps on
-// the GPU (other streams, other host threads) race on the array.
+// All calls share the one array: once a call's arguments have passed their
+// checks, the kernel's per-unit counters are cleared on the stream just before
+// the launch (a rejected call touches nothing), and calls whose work overlaps
+// on the GPU (other streams, other host threads) race on the array.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -56,6 +57,14 @@ vegas_status_t scratch_address(void** out) {
   return VEGAS_OK;
 }
 
+// vegas::ScratchFn: the array on the current device, asked for only once the
+// call's arguments have passed their checks.
+vegas_status_t scratch_workspace(void** ws, size_t* bytes) {
+  vegas_status_t st = scratch_address(ws);
+  if (st == VEGAS_OK) *bytes = kScratchBytes;
+  return st;
+}
+
 }  // namespace
 
 VEGAS_API size_t vegas_verify_noalloc_max_scratch_bytes(void) { return kScratchBytes; }
@@ -64,25 +73,14 @@ VEGAS_API vegas_status_t vegas_verify_attn_capture_noalloc(
     const vegas_paged_kv_t* kv, const void* q, void* out, float* scores, int score_stride,
     const int32_t* ctx_lens, int batch, int gamma, int capture_row_a, int capture_row_b,
     float softmax_scale, void* stream) {
-  if (batch < 0 || gamma < 0)
-    return (vegas_status_t)vegas::record_failure(VEGAS_ERR_INVALID_ARG, "negative batch or gamma");
-  const size_t need = vegas_verify_workspace_size(kv, batch, gamma);
-  if (need > kScratchBytes)
+  // Every argument is checked before the array is touched; its counters are
+  // then cleared on `stream` right before the kernel.
+  vegas_status_t st = vegas::verify_two_rows(kv, q, out, scores, score_stride, ctx_lens, batch,
+                                             gamma, capture_row_a, capture_row_b, softmax_scale,
+                                             nullptr, 0, stream, scratch_workspace);
+  if (st == VEGAS_ERR_WORKSPACE_TOO_SMALL)
     return (vegas_status_t)vegas::record_failure(
-        VEGAS_ERR_WORKSPACE_TOO_SMALL,
-        "this shape needs more split-KV scratch than the fixed 16 MiB array; "
-        "use vegas_verify_attn_capture with a caller-allocated workspace");
-  void* scratch = nullptr;
-  vegas_status_t st = scratch_address(&scratch);
-  if (st != VEGAS_OK) return st;
-  if (need > 0 && batch > 0) {
-    // The per-unit counters (first batch * num_kv_heads ints) must start at zero.
-    const size_t counters = size_t(batch) * (kv ? kv->num_kv_heads : 0) * sizeof(int);
-    cudaError_t e = cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess)
-      return (vegas_status_t)vegas::record_failure(VEGAS_ERR_CUDA, cudaGetErrorString(e));
-  }
-  return vegas_verify_attn_capture(kv, q, out, scores, score_stride, ctx_lens, batch, gamma,
-                                   capture_row_a, capture_row_b, softmax_scale, scratch,
-                                   kScratchBytes, stream);
+        st, "this shape needs more split-KV scratch than the fixed 16 MiB array; "
+            "use vegas_verify_attn_capture with a caller-allocated workspace");
+  return st;
 }

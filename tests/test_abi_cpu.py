@@ -122,3 +122,34 @@ def test_host_validation_of_the_variant_entry_points(vg):
     with pytest.raises(vg.VegasError) as ei:
         vg.vegas_select_topk_shared(16, 9 * 32768, 16, 16, 16, 1, 2, 8, stream=0)
     assert ei.value.status == 2
+
+
+def test_noalloc_checks_every_argument_before_its_scratch(vg):
+    """The no-alloc verify rejects a bad call with the status of the workspace
+    call, before it looks up or clears its scratch array (no device is needed
+    to reach these answers)."""
+    kv = vg.PagedKV(16, 16, 16, 4, 16, 8, 2, 64, 4)
+    with pytest.raises(vg.VegasError) as ei:         # NULL queries
+        vg.vegas_verify_attn_capture_noalloc(kv, None, 16, 16, 64, 16, 1, 4, 0, 4, 0.125,
+                                             stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(vg.VegasError) as ei:         # misaligned output
+        vg.vegas_verify_attn_capture_noalloc(kv, 16, 24, 16, 64, 16, 1, 4, 0, 4, 0.125,
+                                             stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(vg.VegasError) as ei:         # gamma beyond 15: unsupported, not "too small"
+        vg.vegas_verify_attn_capture_noalloc(kv, 16, 16, 16, 64, 16, 1, 16, 0, 16, 0.125,
+                                             stream=0)
+    assert ei.value.status == 2
+    big = vg.PagedKV(16, 16, 16, 4, 16, 64, 2, 128, 4)   # (gamma+1)*G query rows too many
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_verify_attn_capture_noalloc(big, 16, 16, 16, 64, 16, 1, 4, 0, 4, 0.125,
+                                             stream=0)
+    assert ei.value.status == 2
+
+
+def test_bounded_wait_check_limits_are_checked_on_the_host(vg):
+    for bad in (0, -5, 1000001):
+        with pytest.raises(vg.VegasError) as ei:
+            vg.vegas_check_bounded_wait(bad, None, stream=0)
+        assert ei.value.status == 1

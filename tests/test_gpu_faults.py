@@ -58,3 +58,21 @@ def test_small_workspace_is_rejected_on_the_host():
         vg.vegas_verify_attn_capture(c.kv, c.qv, out, None, 1, c.lens_t, 1, c.w.gamma, 0,
                                      c.w.gamma, c.scale, ws, ws.numel())
     assert ei.value.status == 3
+
+
+def test_a_bounded_wait_that_runs_out_reports_a_timeout_and_the_gpu_stays_usable():
+    """The failure-detection protocol end to end: a kernel's wait on a barrier
+    nothing arrives on gives up after its limit (1 ms here), records
+    VEGAS_ERR_DEVICE_TIMEOUT and returns; the host reads it once, the word
+    clears, and the context keeps working."""
+    vg.vegas_read_device_status()
+    outcome = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    vg.vegas_check_bounded_wait(1000, outcome)
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_read_device_status()
+    assert ei.value.status == 6
+    assert int(outcome.item()) == 0             # the wait ran out
+    vg.vegas_read_device_status()               # cleared
+    c = Case(configs.TINY.with_(ctx_lo=100, ctx_hi=100))
+    c.verify()
+    vg.vegas_read_device_status()               # later kernels run normally

@@ -8,7 +8,8 @@ if not torch.cuda.is_available():
 
 import oracle  # noqa: E402
 import self_speculative_sparse_paged_gb300 as vg  # noqa: E402
-from vegas_case import DEV, to_dev  # noqa: E402
+from vegas_case import DEV, Case, tie_band_ok, to_dev  # noqa: E402
+from workload import configs  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -65,8 +66,10 @@ def _run_shared(scores32: np.ndarray, lens, kps, k_max):
     vg.vegas_select_topk_shared(to_dev(scores32), S, to_dev(np.asarray(lens, np.int32)),
                                 to_dev(np.asarray(kps, np.int32)), idx, B, H, k_max)
     vg.vegas_read_device_status()
-    ref = oracle.select_topk_shared_batch(scores32, np.asarray(lens), np.asarray(kps), k_max)
+    # identical keys: the call's stated fp32 head-order sum, taken by both sides
+    ref = oracle.select_topk_shared_batch_f32(scores32, np.asarray(lens), np.asarray(kps), k_max)
     np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+    return idx
 
 
 @pytest.mark.parametrize("L,k,H", [(1, 1, 8), (1000, 37, 8), (32768, 1639, 8),
@@ -81,6 +84,32 @@ def test_select_shared_ties_and_variable_lengths():
     rng = np.random.default_rng(5)
     s = rng.integers(-2, 3, size=(3, 4, 20000)).astype(np.float32)
     _run_shared(s, [20000, 7, 15000], [900, 7, 0], 1000)
+
+
+@pytest.mark.parametrize("w", [configs.TINY,
+                               configs.QWEN3_8B_B8_48K_64K.with_(batch=2, ctx_lo=3000, ctx_hi=6000)],
+                         ids=["tiny", "qwen_b2_3k_6k"])
+def test_select_shared_end_to_end_within_the_tie_band_of_the_exact_sum(w):
+    """GPU capture then GPU shared select, against the method's definition: the
+    fp64 sum over every head of the fp64 oracle's captured logits.  The sets may
+    differ only at positions within the tie band of the k-th exact score."""
+    c = Case(w)
+    _, scores = c.verify()
+    idx = torch.full((w.batch, w.hkv, c.k_max), -7, dtype=torch.int32, device=DEV)
+    vg.vegas_select_topk_shared(scores, c.stride, c.lens_t, c.kps_t, idx, w.batch, w.hkv,
+                                c.k_max)
+    vg.vegas_read_device_status()
+    got = idx.cpu().numpy()
+    kf, _ = c.caches_f64()
+    ref_s = oracle.capture_scores(c.qv_f64(), kf, c.pm.block_table, c.lens, c.scale)
+    ref = oracle.select_topk_shared_batch(ref_s, c.lens, c.kps, c.k_max)
+    for b in range(w.batch):
+        L, k = int(c.lens[b]), int(c.kps[b])
+        summed = oracle.summed_head_scores(ref_s, L, b)
+        assert (got[b] == got[b, 0]).all(), "one T for every KV head"
+        ok, msg = tie_band_ok(got[b, 0, :k], ref[b, 0, :k], summed, k)
+        assert ok, msg
+        assert (got[b, :, k:] == -1).all()
 
 
 # ---------------------------------------------------------------- sliding window (+ sinks)

@@ -399,6 +399,31 @@ def test_shared_selection_ties_match_brute_force(seed):
         assert (idx[0, :, k:] == -1).all()
 
 
+def test_shared_selection_sums_the_heads_exactly_not_in_fp32():
+    """The shared objective is the exact sum over heads: where an fp32 head-order
+    sum loses a term (1e8 + 1 - 1e8 = 0 in fp32), the selection still follows the
+    exact sum, brute-forced here in integers; the fp32 head-order variant (the
+    library call's stated key) picks the other position."""
+    s = np.array([[[1e8, 0.5, 0.0], [1.0, 0.0, 0.0], [-1e8, 0.0, 0.25]]], dtype=np.float32)
+    exact = [sum(int(round(4 * float(s[0, g, i]))) for g in range(3)) for i in range(3)]
+    assert exact == [4, 2, 1]
+    for k in (1, 2):
+        idx = oracle.select_topk_shared_batch(s, np.array([3]), np.array([k]), 3)
+        assert list(idx[0, 0, :k]) == _brute_force_best(exact, k)
+    f32 = oracle.select_topk_shared_batch_f32(s, np.array([3]), np.array([1]), 1)
+    assert list(f32[0, 0]) == [1]          # fp32: 1e8 + 1 - 1e8 -> 0 < 0.5
+    assert oracle.summed_head_scores(s, 3, 0)[0] == 1.0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_shared_selection_f32_key_equals_the_exact_one_on_representable_sums(seed):
+    rng = np.random.default_rng(300 + seed)
+    s = (rng.integers(-512, 513, size=(2, 8, 700)) * 0.125).astype(np.float32)
+    lens, ks = np.array([700, 333]), np.array([35, 17])
+    np.testing.assert_array_equal(oracle.select_topk_shared_batch_f32(s, lens, ks, 40),
+                                  oracle.select_topk_shared_batch(s, lens, ks, 40))
+
+
 def test_shared_selection_with_one_kv_head_is_the_per_head_selection():
     rng = np.random.default_rng(12)
     s = rng.standard_normal((3, 1, 40)).astype(np.float32)
