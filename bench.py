@@ -291,10 +291,9 @@ class GpuIteration:
 class LayerStack:
     """`layers` attention layers of one workload shape resident in HBM, each
     with its own paged cache and queries (the layer's generator streams) under
-    one block table, run as one decode iteration: verify(l) then select(l) for
-    every layer, then every draft step over every layer.  With `pipelined`,
-    select(l) runs on a second stream and overlaps verify(l + 1) (which does not
-    depend on it); draft step 0 of layer l waits for select(l)."""
+    one block table, run as one decode iteration by vegas_decode_iteration:
+    verify(l) then select(l) for every layer, then every draft step over every
+    layer; pipelined, select(l) overlaps verify(l + 1) on a second stream."""
 
     def __init__(self, w, layers, dev):
         import torch
@@ -337,8 +336,10 @@ class LayerStack:
         self.ws = torch.zeros(max(nv, 256), dtype=torch.uint8, device=dev)
         self.kw_t = torch.zeros((w.batch,), dtype=torch.int32, device=dev)
         self.side = torch.cuda.Stream(device=dev)
-        self.ev_v = [torch.cuda.Event() for _ in range(layers)]
-        self.ev_s = [torch.cuda.Event() for _ in range(layers)]
+        self.tails_t = t(np.array([[tl] * w.batch for tl in self.tails], dtype=np.int32))
+        self.layer_descs = [vg.layer(self.kv[i], self.qv[i], self.out_v[i], self.qd[i],
+                                     self.out_d[i], self.scores[i], self.idx[i])
+                            for i in range(layers)]
 
     def step_without_capture(self):
         """The same iteration with verify's capture off and the query-agnostic
@@ -362,32 +363,17 @@ class LayerStack:
                     self.scale, stream=main)
 
     def step(self, pipelined):
+        """One iteration through the library's layer-stack call (select(l) on the
+        side stream, overlapping verify(l + 1), when pipelined)."""
         torch, vg, w = self.torch, self.vg, self.w
-        main = torch.cuda.current_stream()
-        for layer in range(self.layers):
-            vg.vegas_verify_attn_capture(
-                self.kv[layer], self.qv[layer], self.out_v[layer], self.scores[layer],
-                self.stride, self.lens_t, w.batch, w.gamma, 0, w.gamma, self.scale, self.ws,
-                self.ws.numel(), stream=main)
-            sel_stream = self.side if pipelined else main
-            if pipelined:
-                self.ev_v[layer].record(main)
-                self.side.wait_event(self.ev_v[layer])
-            vg.vegas_select_topk(self.scores[layer], self.stride, self.lens_t, self.kps_t,
-                                 self.idx[layer], w.batch, w.hkv, self.k_max, stream=sel_stream)
-            if pipelined:
-                self.ev_s[layer].record(self.side)
-        for j in range(w.gamma):
-            for layer in range(self.layers):
-                if pipelined and j == 0:
-                    main.wait_event(self.ev_s[layer])
-                vg.vegas_sparse_decode_attn(
-                    self.kv[layer], self.qd[layer][j], self.out_d[layer][j], self.idx[layer],
-                    self.k_max, self.kps_t, self.lens_t, self.tl_t[j], self.tails[j], w.batch,
-                    self.scale, stream=main)
+        vg.vegas_decode_iteration(self.layer_descs, self.lens_t, self.kps_t, self.tails_t,
+                                  max(self.tails), w.batch, w.gamma, self.stride, self.k_max,
+                                  self.scale, self.ws, self.ws.numel(),
+                                  stream=torch.cuda.current_stream(),
+                                  select_stream=self.side if pipelined else None)
 
 
-def time_stack(w, layers, dev, stream, reps=10):
+def time_stack(w, layers, dev, stream, verify_plain_us, reps=10):
     """us per iteration of a `layers`-layer stack, serial and with select(l)
     overlapping verify(l + 1) on a second stream (each as a replayed graph)."""
     import torch
@@ -415,9 +401,13 @@ def time_stack(w, layers, dev, stream, reps=10):
     st.vg.vegas_read_device_status(stream)
     out["layers"] = layers
     out["select_hidden_us_per_layer"] = round((out["serial_us"] - out["pipelined_us"]) / layers, 3)
-    # capture + verification-guided select over the query-agnostic baseline, pipelined
+    # capture + verification-guided select over plain verify, pipelined: the
+    # iteration's extra time over the capture-free window-selector iteration,
+    # per plain verify
     out["capture_plus_select_overhead_pipelined"] = round(
-        out["pipelined_us"] / out["no_capture_window_select_us"] - 1.0, 4)
+        (out["pipelined_us"] - out["no_capture_window_select_us"]) / (layers * verify_plain_us), 4)
+    out["overhead_formula"] = ("(pipelined - no-capture window-selector iteration) / "
+                               "(layers x plain verify, back to back)")
     del st
     torch.cuda.empty_cache()
     return out
@@ -473,7 +463,193 @@ def make_events(torch, n, external):
     return None
 
 
-def run_gpu(args, rank, world, dist):
+def graph_of(torch, stream, fn, n):
+    """A CUDA graph of fn(0) .. fn(n - 1) captured on `stream`."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def replay_ms(torch, stream, graph, repeats, reps=1):
+    """Device ms of `repeats` timed regions, each `reps` replays of `graph`,
+    bracketed by CUDA events on the launching stream."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(repeats)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record()
+            for _ in range(reps):
+                graph.replay()
+            b.record()
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def percentile(xs, q):
+    xs = sorted(xs)
+    if len(xs) == 1:
+        return xs[0]
+    pos = q / 100.0 * (len(xs) - 1)
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(xs) - 1)
+    return xs[lo] + (xs[hi] - xs[lo]) * (pos - lo)
+
+
+def stage_times(torch, it, stream, n):
+    """Mean us of verify, select and one draft step from external events at the
+    stage boundaries of a graph of n iterations (the events serialise the stages)."""
+    evs = make_events(torch, n, True)
+    g = graph_of(torch, stream, lambda i: it.step(i % it.R, evs[i]), n)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    v = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n)]
+    s = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n)]
+    d = [evs[i][2].elapsed_time(evs[i][3]) for i in range(n)]
+    return {"verify_us": 1000 * statistics.mean(v), "select_us": 1000 * statistics.mean(s),
+            "draft_us_per_step": 1000 * statistics.mean(d) / max(1, it.w.gamma)}
+
+
+def per_call_us(torch, stream, fn, n=50):
+    """us per call of fn(i) in a graph of n calls replayed after a warm replay
+    (consecutive calls overlap through programmatic dependent launch)."""
+    g = graph_of(torch, stream, fn, n)
+    with torch.cuda.stream(stream):
+        g.replay()
+    return 1000.0 * replay_ms(torch, stream, g, 1)[0] / n
+
+
+def verify_kernel_name(w):
+    """Kernel vegas_verify_attn_capture runs for this shape (with capture)."""
+    cols = ((w.group * (w.gamma + 1) + 1) & ~1) + 2
+    return "verify_tc_kernel" if w.head_dim == 128 and cols <= 32 else "verify_attn_kernel"
+
+
+def measure_workload(w, dev, stream, peak, peak_kind, iters=8, repeats=5):
+    """One extra workload: us and GB/s per iteration (graph of `iters`
+    iterations, median of `repeats` timed replays), the stage breakdown, and the
+    roofline fractions of the verify and draft kernels (bytes per launch over
+    the per-launch time of a graph of back-to-back launches, and over the stage
+    events)."""
+    import torch
+    kv_bytes = w.hkv * 4 * w.head_dim * int(gen.ctx_lens(w).sum())
+    replicas = REPLICAS if kv_bytes < 4 * 129e6 else 1
+    it = GpuIteration(w, replicas, dev)
+    nb = algorithmic_bytes(w, it.lens, it.kps)
+    with torch.cuda.stream(stream):
+        for i in range(2):
+            it.step(i % it.R)
+    stream.synchronize()
+    n = max(iters // replicas, 1) * replicas
+    g = graph_of(torch, stream, lambda i: it.step(i % it.R), n)
+    with torch.cuda.stream(stream):
+        g.replay()
+    ms = [t / n for t in replay_ms(torch, stream, g, repeats)]
+    st = stage_times(torch, it, stream, n)
+    v_b2b = per_call_us(torch, stream, lambda i: it.verify(i % it.R), 4 * replicas)
+    v_plain = per_call_us(torch, stream, lambda i: it.verify(i % it.R, capture=False),
+                          4 * replicas)
+    sel = per_call_us(torch, stream, lambda i: it.select(), 20)
+    d_b2b = per_call_us(torch, stream, lambda i: it.draft(i % it.R, 0), 8 * replicas)
+    it.vg.vegas_read_device_status(stream)
+    med = statistics.median(ms)
+    draft_bytes = nb["draft"][0]
+    out = {
+        "workload": w.name, "description": w.description,
+        "us_per_iteration": round(med * 1000, 2),
+        "us_p10_p90": [round(percentile(ms, 10) * 1000, 2), round(percentile(ms, 90) * 1000, 2)],
+        "value": round(nb["total"] / (med * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "pct_of_8tbs": round(100 * nb["total"] / (med * 1e-3) / 8e12, 2),
+        "bytes_per_iteration": nb["total"],
+        "stages_us": {k: round(v, 3) for k, v in st.items()},
+        "back_to_back_us": {"verify_capture": round(v_b2b, 3), "verify_plain": round(v_plain, 3),
+                            "select": round(sel, 3), "draft_step": round(d_b2b, 3)},
+        "capture_plus_select_overhead": round((v_b2b + sel) / v_plain - 1.0, 4),
+        "roofline_verify": {
+            "kernel": verify_kernel_name(w), "bytes_per_launch": nb["verify"],
+            "frac_back_to_back": round(nb["verify"] / (v_b2b * 1e-6) / 1e9 / peak, 4),
+            "frac_stage_events": round(nb["verify"] / (st["verify_us"] * 1e-6) / 1e9 / peak, 4),
+            "peak": peak, "peak_kind": peak_kind},
+        "roofline_draft": {
+            "kernel": "sparse_decode_kernel", "bytes_per_launch": draft_bytes,
+            "frac_back_to_back": round(draft_bytes / (d_b2b * 1e-6) / 1e9 / peak, 4),
+            "frac_stage_events": round(nb["draft"][-1] / (st["draft_us_per_step"] * 1e-6) / 1e9
+                                       / peak, 4)},
+        "l2": (f"iterations rotate over {replicas} copies of the paged cache" if replicas > 1
+               else "one copy of the paged cache, several times the 129 MB L2"),
+    }
+    del it, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_stack(w, dev, stream, peak, peak_kind, repeats=3):
+    """The full-depth layer stack at one (gamma, k) point: us and GB/s per
+    pipelined iteration through vegas_decode_iteration, the capture-free
+    window-selector baseline, and the verify and draft kernels' roofline
+    fractions (one launch per layer, back to back)."""
+    import torch
+    st = LayerStack(w, w.layers, dev)
+    nb = algorithmic_bytes(w, st.lens, st.kps)
+    total = nb["total"] * w.layers
+    res = {}
+    for name, fn in (("pipelined", lambda i: st.step(True)), ("serial", lambda i: st.step(False)),
+                     ("no_capture_window_select", lambda i: st.step_without_capture())):
+        with torch.cuda.stream(stream):
+            fn(0)
+        stream.synchronize()
+        g = graph_of(torch, stream, fn, 1)
+        with torch.cuda.stream(stream):
+            g.replay()
+        res[name] = statistics.median(replay_ms(torch, stream, g, repeats))
+        del g
+    vg, L = st.vg, w.layers
+
+    def verify_l(i, capture=True):
+        l = i % L
+        vg.vegas_verify_attn_capture(st.kv[l], st.qv[l], st.out_v[l],
+                                     st.scores[l] if capture else None, st.stride, st.lens_t,
+                                     w.batch, w.gamma, 0, w.gamma, st.scale, st.ws, st.ws.numel())
+
+    def draft_l(i):
+        l = i % L
+        vg.vegas_sparse_decode_attn(st.kv[l], st.qd[l][0], st.out_d[l][0], st.idx[l], st.k_max,
+                                    st.kps_t, st.lens_t, st.tl_t[0], st.tails[0], w.batch,
+                                    st.scale)
+    v_us = per_call_us(torch, stream, verify_l, L)
+    vp_us = per_call_us(torch, stream, lambda i: verify_l(i, False), L)
+    d_us = per_call_us(torch, stream, draft_l, L)
+    vg.vegas_read_device_status(stream)
+    med = res["pipelined"]
+    out = {
+        "workload": f"{w.name}_gamma{w.gamma}_k{w.k_pct}pct", "description": w.description,
+        "layers": L, "gamma": w.gamma, "k_pct": w.k_pct,
+        "us_per_iteration": round(med * 1000, 1),
+        "serial_us": round(res["serial"] * 1000, 1),
+        "no_capture_window_select_us": round(res["no_capture_window_select"] * 1000, 1),
+        "value": round(total / (med * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "pct_of_8tbs": round(100 * total / (med * 1e-3) / 8e12, 2),
+        "bytes_per_iteration": total,
+        "capture_plus_select_overhead_pipelined": round(
+            (res["pipelined"] - res["no_capture_window_select"]) * 1000 / (L * vp_us), 4),
+        "overhead_formula": "(pipelined - no-capture window-selector iteration) / "
+                            "(layers x plain verify, back to back)",
+        "roofline_verify": {"kernel": verify_kernel_name(w), "us": round(v_us, 2),
+                            "frac_back_to_back": round(nb["verify"] / (v_us * 1e-6) / 1e9 / peak, 4)},
+        "roofline_draft": {"kernel": "sparse_decode_kernel", "us": round(d_us, 2),
+                           "frac_back_to_back": round(nb["draft"][0] / (d_us * 1e-6) / 1e9 / peak,
+                                                      4)},
+        "peak": peak, "peak_kind": peak_kind,
+        "l2": "36 layers of KV cache (tens of GB): nothing survives in L2 between layers",
+    }
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_gpu(args, rank, world, dist, peak, peak_kind):
     import torch
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
@@ -492,90 +668,59 @@ def run_gpu(args, rank, world, dist):
     stream.synchronize()
     vg.vegas_read_device_status(stream)
 
+    # The timed region is K iterations: `reps` replays of a graph of `chunk`
+    # iterations (no event nodes between the kernels, so each may launch while
+    # its predecessor drains).  It is repeated `repeats` times, each timed on
+    # its own; the line reports the median and the 10th/90th percentiles.
     chunk = max(REPLICAS, min(K, 100) // REPLICAS * REPLICAS)
     reps = max(1, math.ceil(K / chunk))
     K_eff = reps * chunk
-    try:
-        evs = make_events(torch, chunk, True)
-    except TypeError:
-        evs = None
-    # The timed graph has no event nodes between the kernels, so each kernel
-    # may launch while its predecessor drains (programmatic dependent launch);
-    # a second graph with events at the stage boundaries gives the breakdown.
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(chunk):
-            it.step(i % REPLICAS)
-    staged = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(staged, stream=stream):
-        for i in range(chunk):
-            it.step(i % REPLICAS, evs[i] if evs else None)
-    # the same iteration with the capture compiled out of verify (select then
-    # reads the previous scores): the denominator of the capture overhead
-    evp = make_events(torch, chunk, True) if evs else None
-    plain = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(plain, stream=stream):
-        for i in range(chunk):
-            it.step(i % REPLICAS, evp[i] if evp else None, capture=False)
+    graph = graph_of(torch, stream, lambda i: it.step(i % REPLICAS), chunk)
+    plain = graph_of(torch, stream, lambda i: it.step(i % REPLICAS, capture=False), chunk)
     with torch.cuda.stream(stream):
         graph.replay()
-        staged.replay()
         plain.replay()
     stream.synchronize()
+    est_ms = replay_ms(torch, stream, graph, 1, reps)[0]
+    repeats = int(max(50, min(200, 10000.0 / max(est_ms, 1e-3))))
 
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        t0.record()
-        for _ in range(reps):
-            graph.replay()
-        t1.record()
+    region_ms = replay_ms(torch, stream, graph, repeats, reps)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms_total = t0.elapsed_time(t1)
-    # the stage breakdown (event nodes between stages), then plain verify
-    # (capture compiled out), same rotation, for the capture overhead
-    with torch.cuda.stream(stream):
-        staged.replay()
-    p0 = torch.cuda.Event(enable_timing=True)
-    p1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        p0.record()
-        for _ in range(max(1, reps // 2)):
-            plain.replay()
-        p1.record()
-    torch.cuda.synchronize()
+    plain_ms = replay_ms(torch, stream, plain, max(5, repeats // 10), reps)
     clocks = sampler.stop()
     vg.vegas_read_device_status(stream)
-    if evp:
-        verify_plain_us = 1000 * statistics.mean(evp[i][0].elapsed_time(evp[i][1])
-                                                 for i in range(chunk))
-    else:
-        verify_plain_us = float("nan")
 
-    ms_total = max_over_ranks(ms_total, dist, dev)
-    ms_step = ms_total / K_eff
-
-    stages = None
-    if evs:
-        v = [evs[i][0].elapsed_time(evs[i][1]) for i in range(chunk)]
-        s = [evs[i][1].elapsed_time(evs[i][2]) for i in range(chunk)]
-        d = [evs[i][2].elapsed_time(evs[i][3]) for i in range(chunk)]
-        stages = {"verify_us": 1000 * statistics.mean(v), "select_us": 1000 * statistics.mean(s),
-                  "draft_us_per_step": 1000 * statistics.mean(d) / w.gamma,
-                  "source": "external CUDA events at the stage boundaries of a separately "
-                            "replayed graph (events there serialise the stages)"}
+    step_ms = [t / K_eff for t in region_ms]
+    ms_step = max_over_ranks(statistics.median(step_ms), dist, dev)
+    timing = {"repeats": repeats, "steps_per_repeat": K_eff,
+              "ms_per_step_p10": round(percentile(step_ms, 10), 5),
+              "ms_per_step_median": round(statistics.median(step_ms), 5),
+              "ms_per_step_p90": round(percentile(step_ms, 90), 5),
+              "plain_iteration_ms_median": round(statistics.median(plain_ms) / K_eff, 5)}
+    stages = stage_times(torch, it, stream, chunk)
+    stages["source"] = ("external CUDA events at the stage boundaries of a separately "
+                        "replayed graph (events there serialise the stages)")
     e2e = run_e2e(it, stream, min(K_eff, 500), nbytes)
     variants = time_variants(it, stream)
-    variants["layer_stack_8"] = time_stack(w, 8, dev, stream)
-    return it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e, variants
+    variants["layer_stack_8"] = time_stack(w, 8, dev, stream, variants["verify_no_capture_us"])
+    extra = {}
+    if world == 1 and not args.quick:
+        del it
+        torch.cuda.empty_cache()
+        for ew in (configs.QWEN3_8B_B8_48K_64K, configs.GPTOSS_20B_B4_128K):
+            extra[ew.name] = measure_workload(ew, dev, stream, peak, peak_kind)
+        sw = configs.QWEN3_8B_36L_B4_96K_120K.with_(gamma=4, k_pct=5)
+        extra[sw.name + "_gamma4_k5pct"] = measure_stack(sw, dev, stream, peak, peak_kind)
+        it = None
+    return (it, nbytes, ms_step, K_eff, stages, timing, clocks, e2e, variants, extra)
 
 
 def run_e2e(it, stream, steps, nbytes):
@@ -627,53 +772,121 @@ def run_e2e(it, stream, steps, nbytes):
 # ---------------------------------------------------------------------------
 # CPU oracle (the reference arm and the cpu_baseline leg)
 # ---------------------------------------------------------------------------
-class OracleWorkload:
-    """Host fp64 inputs of the workload for the oracle."""
-
-    def __init__(self, w):
-        self.w = w
-        self.lens = gen.ctx_lens(w)
-        self.kps = gen.k_per_seq(w, self.lens)
-        self.pm = gen.page_map(w, self.lens)
-        self.kf = gen.bf16_bits_to_f64(gen.paged_cache_bf16(w, 0, "k", self.lens, self.pm))
-        self.vf = gen.bf16_bits_to_f64(gen.paged_cache_bf16(w, 0, "v", self.lens, self.pm))
-        self.qv = gen.bf16_bits_to_f64(gen.f32_to_bf16_bits(gen.verify_queries_f32(w)))
-        self.qd = gen.bf16_bits_to_f64(gen.f32_to_bf16_bits(gen.draft_queries_f32(w)))
-        self.scale = 1.0 / math.sqrt(w.head_dim)
-
-    def unit_step(self, g):
-        """The oracle iteration restricted to KV head g of every sequence."""
-        import oracle
-        w, G = self.w, self.w.group
-        heads = slice(g * G, (g + 1) * G)
-        sub_k = self.kf[:, g:g + 1]
-        sub_v = self.vf[:, g:g + 1]
-        oracle.iteration(self.qv[:, :, heads], self.qd[:, :, heads], sub_k, sub_v,
-                         self.pm.block_table, self.lens, self.kps, self.scale)
+def oracle_unit_inputs(w, b, g):
+    """fp64 inputs of the iteration restricted to (sequence b, KV head g): the
+    unit's K/V rows (every position the iteration touches) in a one-head paged
+    cache with an identity block table, its G heads' verify and draft queries."""
+    lens = gen.ctx_lens(w)
+    L = int(lens[b])
+    n = int(gen.positions_needed(w, lens)[b])
+    pos = np.arange(n, dtype=np.int64)
+    pages = (n + 15) // 16
+    kc = np.zeros((pages, 1, 16, w.head_dim), dtype=np.float64)
+    vc = np.zeros_like(kc)
+    kc[pos // 16, 0, pos % 16] = gen.bf16_bits_to_f64(gen.kv_rows_bf16(w, 0, "k", b, g, pos, L))
+    vc[pos // 16, 0, pos % 16] = gen.bf16_bits_to_f64(gen.kv_rows_bf16(w, 0, "v", b, g, pos, L))
+    heads = slice(g * w.group, (g + 1) * w.group)
+    qv = gen.bf16_bits_to_f64(gen.f32_to_bf16_bits(gen.verify_queries_f32(w)))[b:b + 1, :, heads]
+    qd = gen.bf16_bits_to_f64(gen.f32_to_bf16_bits(gen.draft_queries_f32(w)))[:, b:b + 1, heads]
+    bt = np.arange(pages, dtype=np.int32)[None, :]
+    k = gen.k_per_seq(w, lens)[b:b + 1]
+    return (qv, qd, kc, vc, bt, lens[b:b + 1], k, 1.0 / math.sqrt(w.head_dim))
 
 
-def time_oracle(w, nbytes, budget_s, min_steps=1, max_steps=None):
-    """Times oracle unit steps (one KV head each) until budget_s or max_steps."""
-    ow = OracleWorkload(w)
-    per_unit = nbytes["total"] / w.hkv
-    ow.unit_step(0)                      # warm-up (imports, caches)
-    times = []
-    t_start = time.perf_counter()
-    i = 0
-    while True:
+def _oracle_worker(conn, w, units):
+    """One host process of the oracle pool: builds its units' inputs once, then
+    runs oracle.iteration over them whenever the parent asks."""
+    import oracle
+    inputs = [oracle_unit_inputs(w, b, g) for b, g in units]
+    conn.send("ready")
+    while conn.recv() == "run":
+        for x in inputs:
+            oracle.iteration(*x)
+        conn.send("done")
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+class OraclePool:
+    """The oracle iteration over every (sequence, KV head) unit of a workload, in
+    parallel on the host cores: one spawned process per core (BLAS single-threaded
+    in each), units dealt round-robin and kept by their process, so a step is
+    one full iteration of the workload."""
+
+    def __init__(self, w, cores=None):
+        import multiprocessing as mp
+        units = [(b, g) for b in range(w.batch) for g in range(w.hkv)]
+        n = max(1, min(len(units), cores or os.cpu_count() or 1))
+        ctx = mp.get_context("spawn")        # safe after CUDA was initialised
+        self.procs, self.conns = [], []
+        for i in range(n):
+            a, bconn = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(bconn, w, units[i::n]), daemon=True)
+            p.start()
+            self.procs.append(p)
+            self.conns.append(a)
+        for c in self.conns:
+            if c.recv() != "ready":
+                raise RuntimeError("oracle worker failed to start")
+        self.cores = n
+        self.units = len(units)
+
+    def step(self) -> float:
+        """Wall seconds of one full iteration (every unit) over the pool."""
         t0 = time.perf_counter()
-        ow.unit_step(i % w.hkv)
-        times.append(time.perf_counter() - t0)
-        i += 1
-        if max_steps is not None and i >= max_steps:
-            break
-        if i >= min_steps and time.perf_counter() - t_start >= budget_s:
-            break
-    dt = statistics.mean(times)
-    return {"value": round(per_unit / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "steps": len(times), "s_per_unit_step": round(dt, 3),
-            "sample": (f"{len(times)} oracle steps, each one full iteration of the workload "
-                       f"restricted to one of its {w.hkv} KV heads (fp64 numpy, one thread)")}
+        for c in self.conns:
+            c.send("run")
+        for c in self.conns:
+            c.recv()
+        return time.perf_counter() - t0
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send("stop")
+            except Exception:
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
+            if p.is_alive():
+                p.terminate()
+
+
+def time_oracle(w, nbytes, budget_s, warmup=1, steps=None, cores=None):
+    """Times full oracle iterations of the workload on the host cores: `warmup`
+    untimed, then `steps` timed (or as many as budget_s allows when steps is None,
+    at least one; a given `steps` is also cut at budget_s)."""
+    pool = OraclePool(w, cores)
+    try:
+        for _ in range(max(0, warmup)):
+            pool.step()
+        times = []
+        t_start = time.perf_counter()
+        while True:
+            times.append(pool.step())
+            if steps is not None and len(times) >= steps:
+                break
+            if time.perf_counter() - t_start >= budget_s:
+                break
+    finally:
+        pool.close()
+    dt = statistics.median(times)
+    return {"value": round(nbytes["total"] / dt / 1e9, 4), "unit": "GB/s", "cores": pool.cores,
+            "kind": "oracle", "steps": len(times), "warmup": max(0, warmup),
+            "s_per_step": round(dt, 4), "cpu_model": cpu_model(),
+            "sample": (f"{len(times)} full iterations of the workload (all {pool.units} "
+                       f"(sequence, KV head) units, fp64 numpy), units spread over "
+                       f"{pool.cores} host processes, one BLAS thread each; median wall time")}
 
 
 # ---------------------------------------------------------------------------
@@ -710,10 +923,12 @@ def base_config(w, lens, kps):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="only the headline workload (no extra workloads)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -726,20 +941,21 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        # At most --steps oracle unit steps (one KV head of the iteration each),
-        # stopped once 150 s of them have run, so the arm ends within minutes.
-        ref = time_oracle(w, nbytes, budget_s=150.0, min_steps=1, max_steps=args.steps)
-        gbs = ref["value"]
-        us = nbytes["total"] / (gbs * 1e9) * 1e6
-        line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
-                "n_gpus": args.gpus, "steps": ref["steps"], "warmup": 1,
-                "ms_per_step": round(us / 1000, 3), "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        # Each step is one full oracle iteration of the workload (all its
+        # (sequence, KV head) units on the host cores); --warmup untimed steps
+        # first, then --steps timed ones, cut at 240 s so the arm ends in minutes.
+        ref = time_oracle(w, nbytes, budget_s=240.0, warmup=args.warmup, steps=args.steps)
+        line = {"impl": "reference", "metric": METRIC, "value": ref["value"], "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": ref["steps"], "warmup": ref["warmup"],
+                "ms_per_step": round(ref["s_per_step"] * 1000, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": base_config(w, lens, kps),
-                "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample")},
-                "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                     "cpu_model")},
+                "e2e": {"value": ref["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0},
-                "note": "fp64 CPU oracle; the pages publish no implementation to install"}
+                "note": "fp64 CPU oracle (the pages publish no implementation to install); "
+                        "ms_per_step is the median wall time of one full iteration"}
         print(json.dumps(line))
         return
 
@@ -748,34 +964,46 @@ def main():
         import torch.distributed as tdist
         tdist.init_process_group("nccl")
         dist = tdist
-    it, nbytes, ms_step, K_eff, stages, verify_plain_us, clocks, e2e, variants = run_gpu(
-        args, rank, world, dist)
+    (it, nbytes, ms_step, K_eff, stages, timing, clocks, e2e, variants, extra) = run_gpu(
+        args, rank, world, dist, peak, peak_kind)
     us_step = ms_step * 1000.0
     gbs = job_gbs(nbytes["total"], ms_step, 1)
     line = {"metric": METRIC, "value": round(job_gbs(nbytes["total"], ms_step, world), 2),
             "unit": "GB/s",
             "n_gpus": world, "steps": K_eff, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 5), "us_per_iteration": round(us_step, 2),
+            "timing": timing,
             "pct_of_8tbs": round(100 * gbs / (ROOFLINE_TBS * 1000), 2),
             "pct_of_measured_hbm": round(100 * gbs / peak, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": base_config(it.w, it.lens, it.kps),
+            "data": "synthetic", "config": base_config(w, lens, kps),
             "bytes_per_iteration": nbytes["total"],
-            "gpu_launches": K_eff * it.launches_per_step, "clocks": clocks, "e2e": e2e}
-    if stages:
-        v_us = stages["verify_us"]
-        line["stages"] = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in stages.items()}
-        line["stages"]["verify_plain_us"] = round(verify_plain_us, 3)
-        line["capture_plus_select_overhead"] = round(
-            (v_us + stages["select_us"]) / verify_plain_us - 1.0, 4)
-        line["roofline"] = roofline_entry(nbytes["verify"], v_us, peak, peak_kind,
-                                          variants.get("verify_capture2_us"))
+            "gpu_launches": K_eff * (2 + w.gamma) * timing["repeats"], "clocks": clocks,
+            "e2e": e2e}
+    v_us = stages["verify_us"]
+    line["stages"] = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in stages.items()}
+    # §8: capture plus top-k over plain verify, back to back (each kernel in a
+    # graph of its own launches), and over the stage events
+    vb2b, vplain = variants["verify_capture2_us"], variants["verify_no_capture_us"]
+    line["capture_plus_select_overhead"] = round((vb2b + variants["select_us"]) / vplain - 1.0, 4)
+    line["capture_overhead"] = round(vb2b / vplain - 1.0, 4)
+    line["overhead_formula"] = ("(verify with capture + select) / plain verify - 1, each "
+                                "timed back to back in a graph of its own launches")
+    line["roofline"] = roofline_entry(nbytes["verify"], v_us, peak, peak_kind, vb2b)
+    line["roofline_draft"] = {
+        "kernel": "sparse_decode_kernel", "bound": "hbm", "bytes_per_launch": nbytes["draft"][-1],
+        "duration_us": round(stages["draft_us_per_step"], 3),
+        "frac": round(nbytes["draft"][-1] / (stages["draft_us_per_step"] * 1e-6) / 1e9 / peak, 4),
+        "duration_source": "stage events around the draft steps, per step"}
     # the "next" rows, measured the same way on the same workload: collect-all
     # capture, one T shared by all heads, the query-agnostic window selector
     line["variants"] = variants
+    if extra:
+        line["workloads"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        ref = time_oracle(it.w, nbytes, budget_s=15.0)
-        line["cpu_baseline"] = {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        ref = time_oracle(w, nbytes, budget_s=15.0, warmup=1)
+        line["cpu_baseline"] = {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                    "cpu_model")}
     if rank == 0:
         print(json.dumps(line))
     if dist:

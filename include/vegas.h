@@ -239,6 +239,50 @@ vegas_status_t vegas_sparse_decode_attn(
     void* stream);
 
 /* ------------------------------------------------------------------------
+ * (4) One decode iteration over a stack of layers (§2 "Core mechanism": each
+ * layer's verify pass selects the entries its next draft phase attends; §4
+ * puts the selection's cost at 5.9-9.4% of decode time).
+ *
+ * For every layer l in order: vegas_verify_attn_capture (capture rows 0 and
+ * gamma) followed by vegas_select_topk on that layer's scores; then, for every
+ * draft step j < gamma and every layer l, vegas_sparse_decode_attn over the
+ * layer's indices and the tail
+ *   [ctx_lens[b], ctx_lens[b] + tail_lens[j * batch + b]).
+ * Layer-pipelined select: when select_stream is not NULL, select(l) runs on
+ * select_stream and overlaps verify(l + 1) on `stream` (which does not depend
+ * on it), and draft step 0 of layer l waits for select(l).  Every piece of
+ * work is joined back into `stream`, so the call can be captured in a CUDA
+ * graph on `stream`.  The cross-stream ordering uses events the library
+ * creates once per device (2 per layer, grown to the largest layer count
+ * seen): make the first call with a given layer count before any capture.
+ * Calls are serialised per device on the host while they enqueue.
+ *
+ *   layers: host array of num_layers descriptors; every layer has the same
+ *           batch, heads and head_dim (one model's stack); block tables may
+ *           be shared.
+ *   ctx_lens, k_per_seq: device int32 [batch] (L_b, k_b), as for verify/select
+ *   tail_lens: device int32 [gamma][batch]; max_tail >= every entry
+ *   workspace: verify workspace of vegas_verify_workspace_size(layer 0) bytes
+ *              (layers run their verify one after another and share it)
+ * Every argument is checked before anything is launched.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  vegas_paged_kv_t kv;          /* this layer's caches */
+  const void* q_verify;         /* device bf16 [batch][gamma + 1][Hq][d], 16-byte aligned */
+  void* out_verify;             /* device bf16, same shape, 16-byte aligned */
+  const void* q_draft;          /* device bf16 [gamma][batch][Hq][d], 16-byte aligned */
+  void* out_draft;              /* device bf16, same shape */
+  float* scores;                /* device fp32 [batch][Hkv][score_stride] */
+  int32_t* idx;                 /* device int32 [batch][Hkv][k_max] */
+} vegas_layer_t;
+
+vegas_status_t vegas_decode_iteration(
+    const vegas_layer_t* layers, int num_layers, const int32_t* ctx_lens,
+    const int32_t* k_per_seq, const int32_t* tail_lens, int max_tail, int batch, int gamma,
+    int score_stride, int k_max, float softmax_scale, void* workspace,
+    size_t workspace_bytes, void* stream, void* select_stream);
+
+/* ------------------------------------------------------------------------
  * Failure-detection check (the paper has no counterpart).
  *
  * Every wait of these kernels on an on-chip barrier (a TMA tile landing, an

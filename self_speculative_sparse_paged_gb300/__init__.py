@@ -21,7 +21,8 @@ __all__ = [
     "VegasError", "PagedKV", "paged_kv", "lib", "library_path",
     "vegas_verify_workspace_size", "vegas_verify_attn_capture", "vegas_select_topk",
     "vegas_sparse_decode_attn", "vegas_synth_paged_kv", "vegas_verify_attn_capture_noalloc",
-    "vegas_verify_noalloc_max_scratch_bytes", "vegas_check_bounded_wait",
+    "vegas_verify_noalloc_max_scratch_bytes", "vegas_check_bounded_wait", "Layer", "layer",
+    "vegas_decode_iteration",
     "vegas_read_device_status", "vegas_status_string", "vegas_last_error_detail",
     "vegas_abi_version",
 ]
@@ -112,6 +113,22 @@ _sparse = _sig("vegas_sparse_decode_attn", _i32,
 _synth = _sig("vegas_synth_paged_kv", _i32,
               [_c_void_p, _i32, _u64, _i32, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p,
                _c_void_p, _u64, _i32, _c_void_p, _c_void_p])
+class Layer(ctypes.Structure):
+    """Mirror of vegas_layer_t."""
+    _fields_ = [
+        ("kv", PagedKV),
+        ("q_verify", ctypes.c_void_p),
+        ("out_verify", ctypes.c_void_p),
+        ("q_draft", ctypes.c_void_p),
+        ("out_draft", ctypes.c_void_p),
+        ("scores", ctypes.c_void_p),
+        ("idx", ctypes.c_void_p),
+    ]
+
+
+_iteration = _sig("vegas_decode_iteration", _i32,
+                  [ctypes.POINTER(Layer), _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _i32,
+                   _i32, _i32, _i32, _f32, _c_void_p, _sz, _c_void_p, _c_void_p])
 _wait_check = _sig("vegas_check_bounded_wait", _i32, [_i32, _c_void_p, _c_void_p])
 _read_status = _sig("vegas_read_device_status", _i32, [_c_void_p])
 _status_string = _sig("vegas_status_string", ctypes.c_char_p, [_i32])
@@ -238,6 +255,25 @@ def vegas_synth_paged_kv(cache, which: int, seed: int, layer: int, owner, num_pa
     _check(_synth(_ptr(cache), which, seed, layer, _ptr(owner), num_pages, num_kv_heads,
                   head_dim, max_pages_per_seq, _ptr(ctx_lens), _ptr(positions), heavy_threshold,
                   heavy_last, _ptr(unit_dir), _stream(stream)))
+
+
+def layer(kv: PagedKV, q_verify, out_verify, q_draft, out_draft, scores, idx) -> Layer:
+    """vegas_layer_t of one layer's tensors."""
+    return Layer(kv, _ptr(q_verify), _ptr(out_verify), _ptr(q_draft), _ptr(out_draft),
+                 _ptr(scores), _ptr(idx))
+
+
+def vegas_decode_iteration(layers, ctx_lens, k_per_seq, tail_lens, max_tail: int, batch: int,
+                           gamma: int, score_stride: int, k_max: int, softmax_scale: float,
+                           workspace, workspace_bytes: int, stream=None,
+                           select_stream=None) -> None:
+    """verify + select for every layer, then every draft step over every layer;
+    select(l) overlaps verify(l + 1) when select_stream is given."""
+    arr = (Layer * len(layers))(*layers)
+    sel = None if select_stream is None else _stream(select_stream)
+    _check(_iteration(arr, len(layers), _ptr(ctx_lens), _ptr(k_per_seq), _ptr(tail_lens),
+                      max_tail, batch, gamma, score_stride, k_max, softmax_scale,
+                      _ptr(workspace), workspace_bytes, _stream(stream), sel))
 
 
 def vegas_check_bounded_wait(limit_us: int, outcome=None, stream=None) -> None:

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/vegas.h"
 #include "../../include/vegas_synth.h"
@@ -384,7 +385,16 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
   const VerifyPlan pl = plan_verify(kv, batch, gamma, sms, scores != nullptr, true);
   const bool needs_ws = pl.splits > 1 && !pl.cluster;
-  if (needs_ws && scratch && (st = scratch(&workspace, &workspace_bytes)) != VEGAS_OK) return st;
+  if (scratch) {
+    // A library-owned scratch serves exactly the shapes whose reported
+    // workspace size fits it, whether or not this launch would use it.
+    if ((st = scratch(&workspace, &workspace_bytes)) != VEGAS_OK) return st;
+    const size_t reported = std::max(plan_verify(kv, batch, gamma, sms, true, true).bytes,
+                                      plan_verify(kv, batch, gamma, sms, false, true).bytes);
+    if (reported > workspace_bytes)
+      return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "verify workspace %zu < %zu bytes",
+                  workspace_bytes, reported);
+  }
   if (needs_ws) {
     if (!workspace || workspace_bytes < pl.bytes)
       return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "verify workspace %zu < %zu bytes",
@@ -607,6 +617,142 @@ VEGAS_API vegas_status_t vegas_synth_paged_kv(void* cache, int which, uint64_t s
                                          heavy_threshold, heavy_last, unit_dir,
                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "synth launch");
+  return VEGAS_OK;
+}
+
+// =========================================================================
+// One decode iteration over a stack of layers (layer-pipelined select)
+// =========================================================================
+namespace {
+
+// Events ordering select(l) between the two streams: 2 per layer, created once
+// per device and reused; a device's calls enqueue one at a time.
+struct EventPool {
+  std::mutex mu;
+  std::vector<cudaEvent_t> ev;
+};
+EventPool g_event_pool[kMaxDevices];
+
+vegas_status_t check_layer(const vegas_layer_t& L, const vegas_layer_t& L0, int i) {
+  vegas_status_t st = check_kv(&L.kv);
+  if (st != VEGAS_OK) {
+    char why[sizeof(g_detail)];
+    std::snprintf(why, sizeof(why), "%s", g_detail);
+    return fail(st, "layer %d: %s", i, why);
+  }
+  if (L.kv.num_q_heads != L0.kv.num_q_heads || L.kv.num_kv_heads != L0.kv.num_kv_heads ||
+      L.kv.head_dim != L0.kv.head_dim || L.kv.max_pages_per_seq != L0.kv.max_pages_per_seq)
+    return fail(VEGAS_ERR_INVALID_ARG, "layer %d: heads, head_dim or max_pages differ from layer 0",
+                i);
+  if (!L.q_verify || !L.out_verify || !L.q_draft || !L.out_draft || !L.scores || !L.idx)
+    return fail(VEGAS_ERR_INVALID_ARG, "layer %d: NULL pointer", i);
+  if (!aligned16(L.q_verify) || !aligned16(L.out_verify) || !aligned16(L.q_draft) ||
+      !aligned16(L.out_draft))
+    return fail(VEGAS_ERR_INVALID_ARG, "layer %d: queries and outputs must be 16-byte aligned", i);
+  return VEGAS_OK;
+}
+
+}  // namespace
+
+VEGAS_API vegas_status_t vegas_decode_iteration(
+    const vegas_layer_t* layers, int num_layers, const int32_t* ctx_lens,
+    const int32_t* k_per_seq, const int32_t* tail_lens, int max_tail, int batch, int gamma,
+    int score_stride, int k_max, float softmax_scale, void* workspace, size_t workspace_bytes,
+    void* stream, void* select_stream) {
+  // ---- every check before the first launch
+  if (!layers || num_layers < 1) return fail(VEGAS_ERR_INVALID_ARG, "no layers");
+  if (!ctx_lens || !k_per_seq || (gamma > 0 && !tail_lens))
+    return fail(VEGAS_ERR_INVALID_ARG, "NULL ctx_lens, k_per_seq or tail_lens");
+  if (batch < 0 || gamma < 0 || max_tail < 0 || k_max < 1 || score_stride < 1)
+    return fail(VEGAS_ERR_INVALID_ARG, "batch %d, gamma %d, max_tail %d, k_max %d, stride %d",
+                batch, gamma, max_tail, k_max, score_stride);
+  if (gamma > 15) return fail(VEGAS_ERR_UNSUPPORTED, "gamma %d (0..15)", gamma);
+  if (!std::isfinite(softmax_scale)) return fail(VEGAS_ERR_INVALID_ARG, "softmax_scale not finite");
+  if (select_stream && select_stream == stream)
+    return fail(VEGAS_ERR_INVALID_ARG, "select_stream must differ from stream (or be NULL)");
+  for (int i = 0; i < num_layers; ++i) {
+    vegas_status_t st = check_layer(layers[i], layers[0], i);
+    if (st != VEGAS_OK) return st;
+  }
+  const vegas_paged_kv_t& kv0 = layers[0].kv;
+  const int G = kv0.num_q_heads / kv0.num_kv_heads;
+  if ((verify_columns((gamma + 1) * G, true) + 7) / 8 > vegas::verify_max_ntiles(kv0.head_dim))
+    return fail(VEGAS_ERR_UNSUPPORTED, "(gamma+1)*G = %d query rows exceeds this head_dim's limit",
+                (gamma + 1) * G);
+  if (G > 16) return fail(VEGAS_ERR_UNSUPPORTED, "group size %d (at most 16)", G);
+  if (k_max + max_tail > vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta)
+    return fail(VEGAS_ERR_UNSUPPORTED, "k_max + max_tail = %d exceeds %d", k_max + max_tail,
+                vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta);
+  if ((long long)score_stride > 8ll * vegas::select_max_chunk())
+    return fail(VEGAS_ERR_UNSUPPORTED, "score_stride %d exceeds %d", score_stride,
+                8 * vegas::select_max_chunk());
+  if (batch == 0) return VEGAS_OK;
+  int dev = 0;
+  {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(VEGAS_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  }
+  vegas_status_t st = device_info(nullptr, nullptr);
+  if (st != VEGAS_OK) return st;
+  const size_t need = vegas_verify_workspace_size(&kv0, batch, gamma);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(VEGAS_ERR_WORKSPACE_TOO_SMALL, "verify workspace %zu < %zu bytes",
+                workspace_bytes, need);
+
+  // ---- enqueue
+  EventPool& pool = g_event_pool[dev];
+  std::lock_guard<std::mutex> lock(pool.mu);
+  const bool piped = select_stream != nullptr;
+  if (piped) {
+    while ((int)pool.ev.size() < 2 * num_layers) {
+      cudaEvent_t e = nullptr;
+      cudaError_t ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+      if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventCreateWithFlags");
+      pool.ev.push_back(e);
+    }
+  }
+  cudaStream_t main_s = static_cast<cudaStream_t>(stream);
+  cudaStream_t side_s = static_cast<cudaStream_t>(select_stream);
+  for (int l = 0; l < num_layers; ++l) {
+    const vegas_layer_t& L = layers[l];
+    st = vegas_verify_attn_capture(&L.kv, L.q_verify, L.out_verify, L.scores, score_stride,
+                                   ctx_lens, batch, gamma, 0, gamma, softmax_scale, workspace,
+                                   workspace_bytes, stream);
+    if (st != VEGAS_OK) return st;
+    if (piped) {
+      cudaError_t ce = cudaEventRecord(pool.ev[2 * l], main_s);
+      if (ce == cudaSuccess) ce = cudaStreamWaitEvent(side_s, pool.ev[2 * l], 0);
+      if (ce != cudaSuccess) return cuda_fail(ce, "verify -> select ordering");
+    }
+    st = vegas_select_topk(L.scores, score_stride, ctx_lens, k_per_seq, L.idx, batch,
+                           L.kv.num_kv_heads, k_max, piped ? select_stream : stream);
+    if (st != VEGAS_OK) return st;
+    if (piped) {
+      cudaError_t ce = cudaEventRecord(pool.ev[2 * l + 1], side_s);
+      if (ce != cudaSuccess) return cuda_fail(ce, "select completion event");
+    }
+  }
+  for (int j = 0; j < gamma; ++j) {
+    for (int l = 0; l < num_layers; ++l) {
+      const vegas_layer_t& L = layers[l];
+      if (piped && j == 0) {
+        cudaError_t ce = cudaStreamWaitEvent(main_s, pool.ev[2 * l + 1], 0);
+        if (ce != cudaSuccess) return cuda_fail(ce, "select -> draft ordering");
+      }
+      const size_t qoff = size_t(j) * batch * L.kv.num_q_heads * L.kv.head_dim * 2;
+      st = vegas_sparse_decode_attn(
+          &L.kv, static_cast<const uint8_t*>(L.q_draft) + qoff,
+          static_cast<uint8_t*>(L.out_draft) + qoff, L.idx, k_max, k_per_seq, ctx_lens,
+          tail_lens + size_t(j) * batch, max_tail, batch, softmax_scale, stream);
+      if (st != VEGAS_OK) return st;
+    }
+  }
+  if (piped && gamma == 0) {
+    // no draft step joined the select stream back: wait for its last select
+    cudaError_t ce = cudaStreamWaitEvent(main_s, pool.ev[2 * (num_layers - 1) + 1], 0);
+    if (ce != cudaSuccess) return cuda_fail(ce, "select join");
+  }
   return VEGAS_OK;
 }
 

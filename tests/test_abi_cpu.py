@@ -1,7 +1,9 @@
 """The C-ABI library loads and exports every declared entry point (no GPU needed).
 
 Only host-side argument validation is exercised here: those calls return a
-status before anything touches a device.
+status before anything touches a device.  They pass made-up addresses, so
+they run only where no GPU is visible: on a GPU machine a validation bug
+would launch a kernel on them.
 """
 import ctypes
 import os
@@ -12,8 +14,18 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def _gpu_visible() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except ImportError:
+        return False
+
+
 @pytest.fixture(scope="module")
 def vg():
+    if _gpu_visible():
+        pytest.skip("made-up device addresses: host-validation tests run only without a GPU")
     import __graft_entry__
     try:
         __graft_entry__.build()
@@ -153,3 +165,23 @@ def test_bounded_wait_check_limits_are_checked_on_the_host(vg):
         with pytest.raises(vg.VegasError) as ei:
             vg.vegas_check_bounded_wait(bad, None, stream=0)
         assert ei.value.status == 1
+
+
+def test_decode_iteration_checks_every_layer_before_launching(vg):
+    kv = vg.PagedKV(16, 16, 16, 4, 16, 8, 2, 64, 4)
+    good = vg.Layer(kv, 16, 16, 16, 16, 16, 16)
+    bad_kv = vg.Layer(vg.PagedKV(16, 16, 16, 4, 16, 8, 2, 96, 4), 16, 16, 16, 16, 16, 16)
+    other_heads = vg.Layer(vg.PagedKV(16, 16, 16, 4, 16, 4, 2, 64, 4), 16, 16, 16, 16, 16, 16)
+    null_idx = vg.Layer(kv, 16, 16, 16, 16, 16, 0)
+    args = (16, 16, 16, 8, 1, 4, 64, 8, 0.125, None, 0)
+    for layers, status in (([good, bad_kv], 2), ([good, other_heads], 1), ([good, null_idx], 1),
+                           ([], 1)):
+        with pytest.raises(vg.VegasError) as ei:
+            vg.vegas_decode_iteration(layers, *args, stream=0)
+        assert ei.value.status == status
+    with pytest.raises(vg.VegasError) as ei:           # gamma beyond 15
+        vg.vegas_decode_iteration([good], 16, 16, 16, 8, 1, 16, 64, 8, 0.125, None, 0, stream=0)
+    assert ei.value.status == 2
+    with pytest.raises(vg.VegasError) as ei:           # the select stream must be another one
+        vg.vegas_decode_iteration([good], *args, stream=5, select_stream=5)
+    assert ei.value.status == 1

@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py's JSON line, checked without a GPU."""
 import math
+import os
 
 import bench
 from workload import configs, gen
@@ -43,10 +44,20 @@ def test_algorithmic_bytes_of_the_bench_workload():
 
 
 def test_cpu_baseline_fields_on_the_tiny_workload():
-    """The cpu_baseline object: the oracle timed on host cores, with its sample stated."""
+    """The cpu_baseline object: full oracle iterations timed on host processes
+    (one per unit, up to the core count), with the sample and CPU stated."""
     w = configs.TINY
     lens = gen.ctx_lens(w)
     nb = bench.algorithmic_bytes(w, lens, gen.k_per_seq(w, lens))
-    r = bench.time_oracle(w, nb, budget_s=0.5, max_steps=2)
-    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["cores"] >= 1
-    assert r["value"] > 0 and r["steps"] == 2 and "KV heads" in r["sample"]
+    r = bench.time_oracle(w, nb, budget_s=30.0, warmup=1, steps=2)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s"
+    assert r["cores"] == min(w.batch * w.hkv, os.cpu_count())
+    assert r["value"] > 0 and r["steps"] == 2 and r["warmup"] == 1
+    assert "full iterations" in r["sample"] and r["cpu_model"]
+
+
+def test_percentiles_and_stage_free_helpers():
+    xs = [5.0, 1.0, 3.0, 2.0, 4.0]
+    assert bench.percentile(xs, 50) == 3.0
+    assert bench.percentile(xs, 10) == 1.4 and bench.percentile(xs, 90) == 4.6
+    assert bench.verify_kernel_name(configs.QWEN3_8B_B1_32K) == "verify_tc_kernel"

@@ -53,12 +53,23 @@ def test_noalloc_matches_workspace_entry_point_twice(w):
 
 
 def test_noalloc_rejects_shapes_beyond_the_scratch():
-    # 512 sequences x 8 KV heads: partials for 4096 units exceed the fixed array.
+    """512 sequences x 8 KV heads: the partials of 4096 units exceed the fixed
+    array.  Every buffer is real and sized for the shape (one cache page that all
+    block-table entries name, ten-token prefixes), so the call could run safely
+    even if the size check were missing; it must refuse instead."""
     big = configs.QWEN3_8B_B8_48K_64K.with_(batch=512, ctx_lo=4000, ctx_hi=4000)
-    kv = vg.PagedKV(256, 256, 256, 256 * 512, 16, big.hq, big.hkv, big.head_dim, 256)
-    assert vg.vegas_verify_workspace_size(kv, big.batch, big.gamma) > \
+    B, T, d = big.batch, big.gamma + 1, big.head_dim
+    k = torch.zeros((1, big.hkv, 16, d), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    bt = torch.zeros((B, 256), dtype=torch.int32, device="cuda")
+    kv = vg.paged_kv(k, v, bt, big.hq)
+    q = torch.zeros((B, T, big.hq, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    lens = torch.full((B,), 10, dtype=torch.int32, device="cuda")
+    assert vg.vegas_verify_workspace_size(kv, B, big.gamma) > \
         vg.vegas_verify_noalloc_max_scratch_bytes()
     with pytest.raises(vg.VegasError) as ei:
-        vg.vegas_verify_attn_capture_noalloc(kv, 256, 256, None, 1, 256, big.batch, big.gamma, 0,
-                                             big.gamma, 0.1, stream=0)
+        vg.vegas_verify_attn_capture_noalloc(kv, q, out, None, 1, lens, B, big.gamma, 0,
+                                             big.gamma, 0.1)
     assert ei.value.status == 3
+    torch.cuda.synchronize()
