@@ -522,9 +522,11 @@ def per_call_us(torch, stream, fn, n=50):
 
 
 def verify_kernel_name(w):
-    """Kernel vegas_verify_attn_capture runs for this shape (with capture)."""
+    """Kernel vegas_verify_attn_capture runs for this shape (with capture): the
+    tcgen05 kernel up to 40 query columns at head_dim 128 and 64 at head_dim 64."""
     cols = ((w.group * (w.gamma + 1) + 1) & ~1) + 2
-    return "verify_tc_kernel" if w.head_dim == 128 and cols <= 32 else "verify_attn_kernel"
+    limit = 40 if w.head_dim == 128 else 64
+    return "verify_tc_kernel" if cols <= limit else "verify_attn_kernel"
 
 
 def measure_workload(w, dev, stream, peak, peak_kind, iters=8, repeats=5):
@@ -653,8 +655,10 @@ def run_gpu(args, rank, world, dist, peak, peak_kind):
     import torch
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    w = WORKLOAD
-    it = GpuIteration(w, REPLICAS, dev)
+    w = configs.BY_NAME[args.workload]
+    kv_bytes = w.hkv * 4 * w.head_dim * int(gen.ctx_lens(w).sum())
+    replicas = REPLICAS if kv_bytes < 4 * 129e6 else 1
+    it = GpuIteration(w, replicas, dev)
     vg = it.vg
     nbytes = algorithmic_bytes(w, it.lens, it.kps)
     stream = torch.cuda.Stream(device=dev)
@@ -663,8 +667,8 @@ def run_gpu(args, rank, world, dist, peak, peak_kind):
     # warm-up: every path once eagerly (configures kernels), then W steps
     with torch.cuda.stream(stream):
         for i in range(max(W, 1)):
-            it.step(i % REPLICAS)
-            it.verify(i % REPLICAS, capture=False)
+            it.step(i % it.R)
+            it.verify(i % it.R, capture=False)
     stream.synchronize()
     vg.vegas_read_device_status(stream)
 
@@ -672,11 +676,11 @@ def run_gpu(args, rank, world, dist, peak, peak_kind):
     # iterations (no event nodes between the kernels, so each may launch while
     # its predecessor drains).  It is repeated `repeats` times, each timed on
     # its own; the line reports the median and the 10th/90th percentiles.
-    chunk = max(REPLICAS, min(K, 100) // REPLICAS * REPLICAS)
+    chunk = max(it.R, min(K, 100) // it.R * it.R)
     reps = max(1, math.ceil(K / chunk))
     K_eff = reps * chunk
-    graph = graph_of(torch, stream, lambda i: it.step(i % REPLICAS), chunk)
-    plain = graph_of(torch, stream, lambda i: it.step(i % REPLICAS, capture=False), chunk)
+    graph = graph_of(torch, stream, lambda i: it.step(i % it.R), chunk)
+    plain = graph_of(torch, stream, lambda i: it.step(i % it.R, capture=False), chunk)
     with torch.cuda.stream(stream):
         graph.replay()
         plain.replay()
@@ -715,8 +719,10 @@ def run_gpu(args, rank, world, dist, peak, peak_kind):
     if world == 1 and not args.quick:
         del it
         torch.cuda.empty_cache()
-        for ew in (configs.QWEN3_8B_B8_48K_64K, configs.GPTOSS_20B_B4_128K):
-            extra[ew.name] = measure_workload(ew, dev, stream, peak, peak_kind)
+        for ew in (configs.QWEN3_8B_B1_32K, configs.QWEN3_8B_B8_48K_64K,
+                   configs.GPTOSS_20B_B4_128K):
+            if ew.name != w.name:
+                extra[ew.name] = measure_workload(ew, dev, stream, peak, peak_kind)
         sw = configs.QWEN3_8B_36L_B4_96K_120K.with_(gamma=4, k_pct=5)
         extra[sw.name + "_gamma4_k5pct"] = measure_stack(sw, dev, stream, peak, peak_kind)
         it = None
@@ -892,13 +898,14 @@ def time_oracle(w, nbytes, budget_s, warmup=1, steps=None, cores=None):
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
-def roofline_entry(bytes_per_launch, duration_us, peak, peak_kind, back_to_back_us=None):
+def roofline_entry(bytes_per_launch, duration_us, peak, peak_kind, back_to_back_us=None,
+                   kernel="verify_tc_kernel"):
     """The bench line's roofline object for the verify kernel: algorithmic bytes
     per launch over its stage-event duration against the HBM peak, the ncu
     traffic while the sources match, and (context) the same bytes over the
     per-launch time of a graph of launches back to back."""
     achieved = bytes_per_launch / (duration_us * 1e-6) / 1e9
-    out = {"kernel": "verify_tc_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+    out = {"kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1),
            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
            "peak_kind": peak_kind, "traffic": verify_traffic_bytes(),
            "bytes_per_launch": bytes_per_launch, "duration_us": round(duration_us, 3),
@@ -912,12 +919,14 @@ def roofline_entry(bytes_per_launch, duration_us, peak, peak_kind, back_to_back_
 
 
 def base_config(w, lens, kps):
+    kv = w.hkv * 4 * w.head_dim * int(lens.sum())
+    reps = REPLICAS if kv < 4 * 129e6 else 1
+    l2 = (f"steps rotate over {reps} copies of the paged KV cache ({reps}x {kv / 1e6:.0f} MB)"
+          if reps > 1 else f"one copy of the paged KV cache ({kv / 1e6:.0f} MB, >4x the 129 MB L2)")
     return {"workload": w.name, "description": w.description, "batch": w.batch,
             "ctx_len": int(lens.max()), "gamma": w.gamma, "k": int(kps.max()),
             "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim, "page_size": 16,
-            "l2": f"steps rotate over {REPLICAS} copies of the paged KV cache "
-                  f"({REPLICAS}x {w.hkv * 4 * w.head_dim * int(lens.max()) / 1e6:.0f} MB)",
-            "parallelism": "replicas"}
+            "l2": l2, "parallelism": "replicas"}
 
 
 def main():
@@ -929,11 +938,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="only the headline workload (no extra workloads)")
+    ap.add_argument("--workload", default=WORKLOAD.name, choices=sorted(configs.BY_NAME),
+                    help="the headline workload (default: the Qwen3-8B layer, batch 1, 32K)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    w = WORKLOAD
+    w = configs.BY_NAME[args.workload]
     lens, kps = gen.ctx_lens(w), gen.k_per_seq(w, gen.ctx_lens(w))
     nbytes = algorithmic_bytes(w, lens, kps)
     peak, peak_kind = read_peaks()
@@ -989,7 +1000,8 @@ def main():
     line["capture_overhead"] = round(vb2b / vplain - 1.0, 4)
     line["overhead_formula"] = ("(verify with capture + select) / plain verify - 1, each "
                                 "timed back to back in a graph of its own launches")
-    line["roofline"] = roofline_entry(nbytes["verify"], v_us, peak, peak_kind, vb2b)
+    line["roofline"] = roofline_entry(nbytes["verify"], v_us, peak, peak_kind, vb2b,
+                                      kernel=verify_kernel_name(w))
     line["roofline_draft"] = {
         "kernel": "sparse_decode_kernel", "bound": "hbm", "bytes_per_launch": nbytes["draft"][-1],
         "duration_us": round(stages["draft_us_per_step"], 3),

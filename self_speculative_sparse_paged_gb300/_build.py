@@ -31,7 +31,8 @@ UNITS = [
     ("vegas_api.cu", "vegas_api.o", []),
     ("synth.cu", "synth.o", []),
     ("verify_noalloc.cu", "verify_noalloc.o", []),
-    ("verify_tc.cu", "verify_tc.o", []),
+    ("verify_tc.cu", "verify_tc_d128.o", ["-DVEGAS_TC_D=128"]),
+    ("verify_tc.cu", "verify_tc_d64.o", ["-DVEGAS_TC_D=64"]),
     ("select_topk.cu", "select_topk.o", []),
     ("select_window.cu", "select_window.o", []),
     ("raw_aggregate.cu", "raw_aggregate.o", []),

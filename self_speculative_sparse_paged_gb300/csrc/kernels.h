@@ -13,7 +13,7 @@ namespace vegas {
 
 constexpr int kAttnWarps = 8;          // warps per attention CTA
 constexpr int kMaxSplits = 128;        // split-KV partials per (sequence, KV head)
-constexpr int kMaxSparseCluster = 8;   // CTAs per (sequence, KV head) in the draft kernel
+constexpr int kMaxSparseCluster = 16;  // CTAs per (sequence, KV head) in the draft kernel
 constexpr int kMaxSparseRowsPerCta = 2048;
 
 struct VerifyParams {
@@ -34,7 +34,9 @@ struct VerifyParams {
   float scale_log2;         // scale * log2(e)
   int pages_per_split;
   int num_splits;
-  int cluster_merge;        // tcgen05 kernel: the splits of a unit form one cluster and merge on chip
+  int cluster_merge;        // tcgen05 kernel: a unit's splits form clusters that merge on chip
+  int cluster_size;         // CTAs per cluster (S); num_splits / S clusters per unit, merged
+                            // across clusters through the workspace when more than one
   int* tickets;
   float* part_ml;
   float* part_o;
@@ -122,21 +124,37 @@ vegas_status_t verify_two_rows(const vegas_paged_kv_t* kv, const void* q, void* 
 
 // Largest 8-row query tile count per head_dim (d=128: 48 rows, d=64: 64 rows).
 inline int verify_max_ntiles(int head_dim) { return head_dim == 128 ? 6 : 8; }
-// tcgen05 verify kernel (head_dim 128, at most 32 query columns incl. capture),
-// streaming 8-page tiles.
-constexpr int kTcMaxColumns = 32;
+// tcgen05 verify kernel (head_dim 128 with at most 40 query columns incl.
+// capture, head_dim 64 with at most 64), streaming 8-page tiles.
+inline int verify_tc_max_columns(int head_dim) { return head_dim == 128 ? 40 : 64; }
 constexpr int kTcPagesPerTile = 8;
 constexpr int kMaxVerifyCluster = 16;   // splits merged on chip (non-portable cluster size)
-cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             const VerifyParams& p, int ncols, bool capture, int batch,
-                             cudaStream_t stream);
+cudaError_t launch_verify_tc_d64(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                 const VerifyParams& p, int ncols, bool capture, int batch,
+                                 cudaStream_t stream);
+cudaError_t launch_verify_tc_d128(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                  const VerifyParams& p, int ncols, bool capture, int batch,
+                                  cudaStream_t stream);
+inline cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                    const VerifyParams& p, int head_dim, int ncols, bool capture,
+                                    int batch, cudaStream_t stream) {
+  return head_dim == 64 ? launch_verify_tc_d64(kmap, vmap, p, ncols, capture, batch, stream)
+                        : launch_verify_tc_d128(kmap, vmap, p, ncols, capture, batch, stream);
+}
 // Clusters of `cluster` CTAs of the tcgen05 kernel resident at once (0: none / error).
-int verify_tc_max_active_clusters(int ncols, bool capture, int cluster);
+int verify_tc_max_active_clusters_d64(int ncols, bool capture, int cluster);
+int verify_tc_max_active_clusters_d128(int ncols, bool capture, int cluster);
+inline int verify_tc_max_active_clusters(int head_dim, int ncols, bool capture, int cluster) {
+  return head_dim == 64 ? verify_tc_max_active_clusters_d64(ncols, capture, cluster)
+                        : verify_tc_max_active_clusters_d128(ncols, capture, cluster);
+}
 template <int D, bool CAP>
 cudaError_t launch_verify_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
                             const VerifyParams& p, int ntiles, int batch, cudaStream_t stream);
 
 size_t sparse_smem_bytes(int head_dim, int ntiles);
+// Clusters of `cluster` draft-kernel CTAs resident at once (0: none / error).
+int sparse_max_active_clusters(int head_dim, int ntiles, int cluster);
 cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int batch,
                           cudaStream_t stream);
 

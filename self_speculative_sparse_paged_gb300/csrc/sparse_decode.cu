@@ -88,6 +88,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   const int unit = b * p.hkv + g;
   const int cap = p.max_pages * 16;
 
+  // The selected positions of this CTA's range are requested together with
+  // k_b and the tail (entries past k_b are replaced below), so the index and
+  // length loads take one round trip.
+  constexpr int kPer = SparseCfg<D>::kMaxRows / NTH;
+  const int rbeg = rank * p.rows_per_split;
+  int pos[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = tid + u * NTH, e = rbeg + i;
+    pos[u] = (i < p.rows_per_split && e < p.k_max) ? __ldcg(&p.idx[size_t(unit) * p.k_max + e]) : 0;
+  }
   int kb = p.k_per_seq[b];
   if (kb < 0 || kb > p.k_max) {
     if (tid == 0 && g == 0 && rank == 0) set_error(p.err, kErrDeviceFault);
@@ -96,12 +107,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   const int tstart = p.tail_start[b];
   const int tlen = max(0, p.tail_len[b]);
   const int total = kb + tlen;
-  const int rbeg = rank * p.rows_per_split;
   const int rend = min(rbeg + p.rows_per_split, total);
   const int nrows = max(0, rend - rbeg);
 
-  // The draft queries are requested first, so their load overlaps the index
-  // and block-table loads below (one 16-byte chunk per thread).
+  // The draft queries are requested with the indices and lengths, so their
+  // load overlaps the block-table loads below (one 16-byte chunk per thread).
   constexpr int QCH = NPAD * (D / 8);
   static_assert(QCH <= NTH, "one Q chunk per thread");
   uint4 qchunk = make_uint4(0, 0, 0, 0);
@@ -116,16 +126,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
     fence_mbar_init();
   }
   // Entry e of the list: T[e] for e < k_b, else tail_start + (e - k_b).
-  // Resolved in batches: every index load of a thread, then every page load.
-  constexpr int kPer = SparseCfg<D>::kMaxRows / NTH;
+  // Resolved in batches: every index of a thread (loaded above), then every
+  // page load.
   {
-    int pos[kPer], phys[kPer];
+    int phys[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int i = tid + u * NTH;
       const int e = rbeg + i;
-      pos[u] = 0;
-      if (i < nrows) pos[u] = e < kb ? __ldcg(&p.idx[size_t(unit) * p.k_max + e]) : tstart + (e - kb);
+      if (i >= nrows) pos[u] = 0;
+      else if (e >= kb) pos[u] = tstart + (e - kb);
     }
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
@@ -284,13 +294,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   }
 }
 
+// Launches, or with `clusters` set, reports how many clusters of p.num_splits
+// CTAs can be resident at once.
 template <int D, int NT>
-static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStream_t stream) {
+static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStream_t stream,
+                                     int* clusters = nullptr) {
   constexpr size_t smem = sparse_smem_layout_bytes<D, NT>();
   static std::atomic<uint32_t> configured{0};
   cudaError_t e = once_per_device(configured, [] {
+    cudaError_t r = cudaFuncSetAttribute(sparse_decode_kernel<D, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r != cudaSuccess) return r;
     return cudaFuncSetAttribute(sparse_decode_kernel<D, NT>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -306,21 +322,51 @@ static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStrea
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = clusters ? 1 : 2;
+  if (clusters) return cudaOccupancyMaxActiveClusters(clusters, sparse_decode_kernel<D, NT>, &cfg);
   return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<D, NT>, p);
+}
+
+static cudaError_t launch_sparse_any(const SparseParams& p, int head_dim, int ntiles, int batch,
+                                     cudaStream_t stream, int* clusters) {
+  if (p.num_splits < 1 || p.num_splits > kMaxSparseCluster) return cudaErrorInvalidValue;
+  if (head_dim == 128) {
+    if (ntiles == 1) return launch_sparse_one<128, 1>(p, batch, stream, clusters);
+    if (ntiles == 2) return launch_sparse_one<128, 2>(p, batch, stream, clusters);
+  } else if (head_dim == 64) {
+    if (ntiles == 1) return launch_sparse_one<64, 1>(p, batch, stream, clusters);
+    if (ntiles == 2) return launch_sparse_one<64, 2>(p, batch, stream, clusters);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_sparse(const SparseParams& p, int head_dim, int ntiles, int batch,
                           cudaStream_t stream) {
-  if (p.num_splits < 1 || p.num_splits > kMaxSparseCluster) return cudaErrorInvalidValue;
-  if (head_dim == 128) {
-    if (ntiles == 1) return launch_sparse_one<128, 1>(p, batch, stream);
-    if (ntiles == 2) return launch_sparse_one<128, 2>(p, batch, stream);
-  } else if (head_dim == 64) {
-    if (ntiles == 1) return launch_sparse_one<64, 1>(p, batch, stream);
-    if (ntiles == 2) return launch_sparse_one<64, 2>(p, batch, stream);
+  return launch_sparse_any(p, head_dim, ntiles, batch, stream, nullptr);
+}
+
+int sparse_max_active_clusters(int head_dim, int ntiles, int cluster) {
+  if (cluster < 1 || cluster > kMaxSparseCluster || ntiles < 1 || ntiles > 2) return 0;
+  constexpr int kDevices = 32;
+  // [device][head_dim 64/128][ntiles][cluster]: 0 unknown, -1 none, else the count
+  static std::atomic<int> cache[kDevices][2][3][kMaxSparseCluster + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return 0;
+  std::atomic<int>& slot = cache[dev][head_dim == 128 ? 1 : 0][ntiles][cluster];
+  int c = slot.load(std::memory_order_acquire);
+  if (c == 0) {
+    SparseParams p{};
+    p.hkv = 1;
+    p.num_splits = cluster;
+    int n = 0;
+    if (launch_sparse_any(p, head_dim, ntiles, 1, 0, &n) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    c = n > 0 ? n : -1;
+    slot.store(c, std::memory_order_release);
   }
-  return cudaErrorInvalidValue;
+  return c > 0 ? c : 0;
 }
 
 }  // namespace vegas

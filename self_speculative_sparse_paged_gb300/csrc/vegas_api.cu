@@ -161,7 +161,9 @@ int verify_splits(int units, int max_pages, int sms) {
 struct VerifyPlan {
   int nq, ncols, ntiles, splits, pages_per_split;
   bool tc;        // tcgen05 kernel (head_dim 128, <= 32 columns) instead of the mma.sync one
-  bool cluster;   // tcgen05 kernel with the splits of a unit in one cluster: no workspace
+  bool cluster;   // tcgen05 kernel with a unit's splits in clusters merging on chip
+  int cluster_size;   // CTAs per cluster; splits / cluster_size clusters per unit
+  bool needs_ws;      // partials or tickets go through the workspace
   size_t tickets_off, ml_off, o_off, bytes;
 };
 
@@ -176,22 +178,49 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
   pl.nq = (gamma + 1) * G;
   pl.ncols = verify_columns(pl.nq, capture);
   pl.ntiles = (pl.ncols + 7) / 8;
-  pl.tc = kv->head_dim == 128 && pl.ncols <= vegas::kTcMaxColumns;
+  pl.tc = pl.ncols <= vegas::verify_tc_max_columns(kv->head_dim);
   const int units = std::max(1, batch * kv->num_kv_heads);
   if (pl.tc && units < sms && with_device) {
-    // One cluster per unit, every CTA resident (one wave), >= one tile per split;
-    // the splits merge through distributed shared memory.
-    int S = std::min(std::min(vegas::kMaxVerifyCluster, sms / units),
-                     std::max(1, kv->max_pages_per_seq / vegas::kTcPagesPerTile));
-    while (S > 1 && vegas::verify_tc_max_active_clusters(pl.ncols, capture, S) < units) --S;
-    if (S > 1) {
-      pl.pages_per_split = (kv->max_pages_per_seq + S - 1) / S;
-      pl.splits = (kv->max_pages_per_seq + pl.pages_per_split - 1) / pl.pages_per_split;
+    // C clusters of S CTAs per unit, every CTA resident (one wave), >= one tile
+    // per split, as many CTAs as fit (larger clusters first on ties): a
+    // cluster's splits merge through distributed shared memory, the clusters of
+    // a unit through a few rows of the workspace.
+    const int max_splits = std::max(1, kv->max_pages_per_seq / vegas::kTcPagesPerTile);
+    int bestS = 0, bestC = 0;
+    for (int S = std::min(vegas::kMaxVerifyCluster, sms / units); S >= 2; --S) {
+      const int resident =
+          vegas::verify_tc_max_active_clusters(kv->head_dim, pl.ncols, capture, S);
+      // (the cross-cluster merge takes one lane per cluster: C <= 32)
+      int C = std::min(std::min(sms / (units * S), max_splits / S), 32);
+      while (C > 0 && resident < units * C) --C;
+      if (C > 0 && S * C > bestS * bestC) {
+        bestS = S;
+        bestC = C;
+      }
+    }
+    if (bestS > 1) {
+      // split s takes pages [s * max_pages / n, (s + 1) * max_pages / n): >= 8 each
+      const int n = bestS * bestC;
+      pl.splits = n;
+      pl.pages_per_split = (kv->max_pages_per_seq + n - 1) / n;
       pl.cluster = true;
-      return pl;   // bytes = 0
+      pl.cluster_size = bestS;
+      const int C = bestC;
+      if (C > 1) {
+        pl.needs_ws = true;
+        pl.tickets_off = 0;
+        pl.ml_off = align256(size_t(units) * bestS * 4);
+        pl.o_off = pl.ml_off + align256(size_t(units) * C * pl.nq * 2 * 4);
+        pl.bytes = pl.o_off + size_t(units) * C * pl.nq * kv->head_dim * 4;
+      }
+      return pl;   // bytes = 0 with one cluster per unit
     }
   }
+  pl.cluster_size = 1;
   pl.splits = verify_splits(units, kv->max_pages_per_seq, sms);
+  // the last-arriving tcgen05 CTA stages 3 floats per (partial, row) of its
+  // unit in the freed K/V rings: at most 2 * splits * nq * 12 bytes <= 96 KB
+  if (pl.tc) pl.splits = std::max(1, std::min(pl.splits, 96 * 1024 / (24 * pl.nq)));
   pl.pages_per_split = (kv->max_pages_per_seq + pl.splits - 1) / pl.splits;
   // splits cover whole tiles: 8 pages (tcgen05 kernel) or page pairs
   const int quantum = pl.tc ? vegas::kTcPagesPerTile : 2;
@@ -203,6 +232,7 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
   pl.ml_off = align256(size_t(units) * 4);
   pl.o_off = pl.ml_off + align256(size_t(units) * parts * pl.nq * 2 * 4);
   pl.bytes = pl.o_off + size_t(units) * parts * pl.nq * kv->head_dim * 4;
+  pl.needs_ws = pl.splits > 1;
   return pl;
 }
 
@@ -210,19 +240,29 @@ struct SparsePlan {
   int ntiles, cluster, rows_per_cta;
 };
 
-// One cluster of up to 8 CTAs per (sequence, KV head), each CTA at least 64
-// entries of the list (fewer CTAs when the list is short or the units many).
+// One cluster per (sequence, KV head).  Few units (fewer than half the SMs):
+// the largest cluster (up to 16 CTAs, each at least 64 entries of the list)
+// whose clusters are all resident at once, so every SM gathers.  Many units:
+// one wave of units x cluster <= SMs when every CTA's share fits its row
+// table, else the fewest CTAs that fit it.
 SparsePlan plan_sparse(const vegas_paged_kv_t* kv, int batch, int k_max, int max_tail, int sms) {
   SparsePlan pl{};
   const int G = kv->num_q_heads / kv->num_kv_heads;
   pl.ntiles = (G + 7) / 8;
   const int units = std::max(1, batch * kv->num_kv_heads);
   const int rows_max = std::max(1, k_max + max_tail);
-  int cl = std::min(vegas::kMaxSparseCluster, std::max(1, (rows_max + 63) / 64));
-  while (cl > 1 && (long long)units * (cl / 2) >= 2LL * sms &&
-         (rows_max + cl / 2 - 1) / (cl / 2) <= vegas::kMaxSparseRowsPerCta)
-    cl /= 2;
-  int rpc = (rows_max + cl - 1) / cl;
+  const int fit = (rows_max + vegas::kMaxSparseRowsPerCta - 1) / vegas::kMaxSparseRowsPerCta;
+  int cl;
+  if (2 * units < sms) {
+    cl = std::min(vegas::kMaxSparseCluster, std::max(fit, std::min(sms / units,
+                                                                   (rows_max + 63) / 64)));
+    while (cl > std::max(fit, 1) &&
+           vegas::sparse_max_active_clusters(kv->head_dim, pl.ntiles, cl) < units)
+      --cl;
+  } else {
+    cl = std::max(fit, std::min(vegas::kMaxSparseCluster, std::max(1, sms / units)));
+  }
+  const int rpc = (rows_max + cl - 1) / cl;
   pl.rows_per_cta = (rpc + 15) / 16 * 16;
   pl.cluster = cl;
   return pl;
@@ -384,7 +424,7 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   int sms = 0;
   if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
   const VerifyPlan pl = plan_verify(kv, batch, gamma, sms, scores != nullptr, true);
-  const bool needs_ws = pl.splits > 1 && !pl.cluster;
+  const bool needs_ws = pl.needs_ws;
   if (scratch) {
     // A library-owned scratch serves exactly the shapes whose reported
     // workspace size fits it, whether or not this launch would use it.
@@ -428,6 +468,7 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   p.pages_per_split = pl.pages_per_split;
   p.num_splits = pl.splits;
   p.cluster_merge = pl.cluster ? 1 : 0;
+  p.cluster_size = pl.cluster ? pl.cluster_size : 1;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.tickets = ws ? reinterpret_cast<int*>(ws + pl.tickets_off) : nullptr;
   p.part_ml = ws ? reinterpret_cast<float*>(ws + pl.ml_off) : nullptr;
@@ -435,12 +476,13 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
   p.err = err;
   if (needs_ws && scratch) {
     // shared scratch: its per-unit counters may hold anything from an earlier call
-    cudaError_t e = cudaMemsetAsync(p.tickets, 0, size_t(batch) * kv->num_kv_heads * sizeof(int),
+    const size_t tickets = size_t(batch) * kv->num_kv_heads * (pl.cluster ? pl.cluster_size : 1);
+    cudaError_t e = cudaMemsetAsync(p.tickets, 0, tickets * sizeof(int),
                                     static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
   }
   cudaError_t e =
-      pl.tc ? vegas::launch_verify_tc(km, vm, p, pl.ncols, scores != nullptr, batch,
+      pl.tc ? vegas::launch_verify_tc(km, vm, p, kv->head_dim, pl.ncols, scores != nullptr, batch,
                                       static_cast<cudaStream_t>(stream))
             : launch_verify_any(km, vm, p, kv->head_dim, pl.ntiles, scores != nullptr, batch,
                                 static_cast<cudaStream_t>(stream));

@@ -1,5 +1,6 @@
 // Verify attention with Collect-2-Query capture on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory), head_dim 128.
+// cores (tcgen05, accumulators in tensor memory), head_dim 128 or 64 (this
+// file is compiled once per head_dim, VEGAS_TC_D).
 //
 // Same contract as the mma.sync kernel in verify_attn.cu ("Vegas:
 // Self-Speculative Decoding with Verification-Guided Sparse Attention",
@@ -36,33 +37,47 @@
 #include <cooperative_groups.h>
 
 #include "kernels.h"
+
+#ifndef VEGAS_TC_D
+#error "compile with -DVEGAS_TC_D=64 or -DVEGAS_TC_D=128"
+#endif
 #include "split_merge.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace vegas {
 
-template <int NQP, int NQC>
+template <int D, int NQP, int NQC>
 struct TcCfg {
-  static constexpr int D = 128;
   // K and V tiles live in separate rings: a K slot frees when its S MMA
   // completes, a V slot only when its PV MMA does.  Under full HBM load a
   // tile's load latency reaches ~2 us, which each ring must cover on its own.
-  static constexpr int KS = 3;
+  // (Two K slots when 64 query columns at head_dim 128 leave no room for three.)
+  static constexpr int KS = (D == 128 && NQP == 64) ? 2 : 3;
   static constexpr int VS = 3;
-  static constexpr int kKV = 128 * D * 2;            // one K (or V) tile, 32 KB
-  static constexpr int kQ = 2 * NQP * 128;           // Q^T operand [half][NQP][128 B]
+  static constexpr int kHalves = D / 64;             // 64-column (128-byte) halves of a row
+  static constexpr int kKV = 128 * D * 2;            // one K tile (and the loaded part of V)
+  // A V slot always spans 128 head dimensions (two halves): at head_dim 64 the
+  // PV MMA keeps M = 128 with an upper half that is written once, all zeros
+  // except dimension 64, which holds ones so that O^T row 64 accumulates the
+  // column sums of P.
+  static constexpr int kVS = 128 * 128 * 2;
+  static constexpr bool kOnesRow = D == 64;
+  static constexpr int kQ = kHalves * NQP * 128;     // Q^T operand [half][NQP][128 B]
   static constexpr int kP = 2 * NQP * 128;           // P^T operand [kblock][NQP][128 B]
   static constexpr int kThreads = 384;               // 12 warps
-  static constexpr uint32_t kTmemCols = 128;         // S0, S1, O0, O1 at columns 0, 32, 64, 96
+  static constexpr int kCol = NQP < 32 ? 32 : NQP;   // tensor-memory columns per accumulator
+  static constexpr uint32_t kTmemCols = 4 * kCol;    // S0, S1, O0, O1
   static constexpr int kOffV = KS * kKV;
-  static constexpr int kOffQ = (KS + VS) * kKV;
+  static constexpr int kOffQ = kOffV + VS * kVS;
   static constexpr int kOffP = kOffQ + kQ;
   static constexpr int kOffBar = kOffP + 2 * kP;
   static constexpr int kNumBars = 2 * KS + 2 * VS + 4 * 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  // misc: tmem slot, flag, votes[2][4], colmax[2][4][NQC], colsum[2][4][NQC], tlim[NQP]
-  static constexpr size_t kMisc = 16 + 32 + 4 * (16 * NQC + 2 * NQP);
+  // misc: tmem slot, flag, votes[2][4], colmax[2][4][NQC], colsum[2][4][NQC], tlim[NQP],
+  // rawrow[NQP], running maxima mrun[2][NQC] (kept there instead of registers when NQC > 32)
+  static constexpr size_t kMisc = 16 + 32 + 4 * (18 * NQC + 2 * NQP);
+  static constexpr bool kSmemMax = NQC > 32;
   static constexpr size_t kSmem = size_t(kOffMisc) + kMisc + 1024;
 };
 
@@ -73,16 +88,18 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int NQP, int NQC, bool CAPTURE>
+template <int D, int NQP, int NQC, bool CAPTURE>
 __global__ void __launch_bounds__(384, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const VerifyParams p) {
-  using Cfg = TcCfg<NQP, NQC>;
-  constexpr int D = 128;
+  using Cfg = TcCfg<D, NQP, NQC>;
   constexpr int KS = Cfg::KS;
   constexpr int VS = Cfg::VS;
-  static_assert(NQP == 16 || NQP == 32, "MMA N");
+  constexpr int kCol = Cfg::kCol;
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(NQP == 16 || NQP == 32 || NQP == 64, "MMA N");
   static_assert(NQC % 8 == 0 && NQC <= NQP, "processed columns");
+  static_assert(Cfg::kSmem <= 227 * 1024, "shared memory");
 
   griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -111,6 +128,7 @@ __global__ void __launch_bounds__(384, 1)
   float* colsum = colmax + 8 * NQC;                              // [2][4][NQC]
   int* tlim = reinterpret_cast<int*>(colsum + 8 * NQC);          // [NQP]
   int* rawrow = tlim + NQP;                                      // [NQP] raw-logit row of a column, or -1
+  float* mrun = reinterpret_cast<float*>(rawrow + NQP);          // [2][NQC] running maxima (wide tiles)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -147,13 +165,14 @@ __global__ void __launch_bounds__(384, 1)
   // Warps 1-9 request their chunks of the window queries first, so those
   // loads are in flight together with the context-length load below.
   constexpr int SN = 288;                      // threads of warps 1..9
-  constexpr int QPER = (NQP * 16 + SN - 1) / SN;
+  constexpr int CPR = D / 8;                   // 16-byte chunks per query row
+  constexpr int QPER = (NQP * CPR + SN - 1) / SN;
   uint4 qreg[QPER];
 #pragma unroll
   for (int u = 0; u < QPER; ++u) {
-    const int i = tid - 32 + u * SN, n = i >> 4, c = i & 15;
+    const int i = tid - 32 + u * SN, n = i / CPR, c = i % CPR;
     qreg[u] = make_uint4(0, 0, 0, 0);
-    if (warp >= 1 && warp <= 9 && i < NQP * 16 && n < p.nq) {
+    if (warp >= 1 && warp <= 9 && i < NQP * CPR && n < p.nq) {
       const int t = n / p.group, hl = n - t * p.group;
       qreg[u] = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
                                                ((size_t(b) * T + t) * p.hq + g * p.group + hl) * D)[c];
@@ -173,7 +192,13 @@ __global__ void __launch_bounds__(384, 1)
   const bool is_k = warp == 11 ? half == 0 : warp == 0;
   const bool arms = warp != 11;
   const int pf = warp == 11 ? 6 : 0, np = warp == 11 ? 2 : 6;
-  const int pbeg = split * p.pages_per_split;
+  // Clustered splits share the unit's pages evenly; workspace splits take
+  // pages_per_split each (whole tiles).
+  // (split * max_pages < 2^31: max_pages < 2^20, splits <= 128)
+  const int pbeg = p.cluster_merge ? split * p.max_pages / p.num_splits
+                                   : split * p.pages_per_split;
+  const int pnext = p.cluster_merge ? (split + 1) * p.max_pages / p.num_splits
+                                    : pbeg + p.pages_per_split;
   const int32_t* bt_row = p.block_table + size_t(b) * p.max_pages;
   // Block-table entries are prefetched four tiles ahead, one register per
   // tile modulo 4, so a load is consumed four iterations after its issue.
@@ -198,7 +223,7 @@ __global__ void __launch_bounds__(384, 1)
     L = max(0, min(L, cap - T));
   }
   const int npages = (L + T + 15) / 16;
-  const int pend = min(pbeg + p.pages_per_split, npages);
+  const int pend = min(pnext, npages);
   const int ntiles = pend > pbeg ? (pend - pbeg + 7) / 8 : 0;
   const int cap0 = (p.nq + 1) & ~1;
   const int last_valid = L + p.gamma;
@@ -213,10 +238,20 @@ __global__ void __launch_bounds__(384, 1)
     // (k / 64) * NQP * 128 + n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16 + (k % 8) * 2.
 #pragma unroll
     for (int u = 0; u < QPER; ++u) {
-      const int i = st + u * SN, n = i >> 4, c = i & 15;
-      if (i < NQP * 16)
+      const int i = st + u * SN, n = i / CPR, c = i % CPR;
+      if (i < NQP * CPR)
         *reinterpret_cast<uint4*>(qs + (c >> 3) * (NQP * 128) + n * 128 + (((c & 7) ^ (n & 7)) << 4)) =
             qreg[u];
+    }
+    if constexpr (Cfg::kOnesRow) {
+      // the upper half of every V slot: zeros, and ones at head dimension 64
+      // (element (pos, 64) of the MN-major swizzled half sits at chunk pos % 8)
+      for (int e = st; e < VS * 128 * 8; e += SN) {
+        const int sl = e / (128 * 8), pos = (e / 8) % 128, ch = e % 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (ch == (pos & 7)) v.x = 0x3F80u;   // bf16 1.0 in the chunk's first element
+        *reinterpret_cast<uint4*>(smem + Cfg::kOffV + sl * Cfg::kVS + 16384 + pos * 128 + ch * 16) = v;
+      }
     }
     for (int n = st; n < NQP; n += SN) {
       tlim[n] = n < p.nq ? min(n / p.group, p.gamma) : -1;
@@ -273,6 +308,7 @@ __global__ void __launch_bounds__(384, 1)
     const int depth = is_k ? KS : VS;
     const CUtensorMap* map = is_k ? &kmap : &vmap;
     const uint32_t ring = sbase + (is_k ? 0 : Cfg::kOffV);
+    const uint32_t slot_bytes = is_k ? Cfg::kKV : Cfg::kVS;
     // The cache is streamed once per pass: its lines leave L2 first, so the
     // scores, queries and block table stay there for the kernels after this.
     const uint64_t stream_pol = l2_evict_first_policy();
@@ -306,9 +342,9 @@ __global__ void __launch_bounds__(384, 1)
           __syncwarp(hmask);
           if (hl < np) {
             const int row = (phys * p.hkv + g) * 16;
-            const uint32_t dst = ring + s * Cfg::kKV + (pf + hl) * 2048;
+            const uint32_t dst = ring + s * slot_bytes + (pf + hl) * 2048;
             tma_load_2d_hint(dst, map, 0, row, full, stream_pol);
-            tma_load_2d_hint(dst + 16384, map, 64, row, full, stream_pol);
+            if constexpr (D == 128) tma_load_2d_hint(dst + 16384, map, 64, row, full, stream_pol);
           }
           __syncwarp(hmask);
           issued = t + 1;
@@ -326,7 +362,7 @@ __global__ void __launch_bounds__(384, 1)
     // The whole warp runs the loop, so its control flow and the operand
     // descriptors stay warp-uniform; one elected lane issues and commits.
     constexpr uint32_t idS = idesc_bf16(128, NQP, 0, 0);
-    constexpr uint32_t idPV = idesc_bf16(128, NQP, 1, 0);
+    constexpr uint32_t idPV = idesc_bf16(128, NQP, 1, 0);   // M = 128 dims (padded at D = 64)
     const bool leader = elect_one();
     // Descriptors without their start address; the address field (bits 0-13)
     // holds (address / 16) mod 2^14, the part of a shared-window address the
@@ -343,12 +379,12 @@ __global__ void __launch_bounds__(384, 1)
       if (!wait_all(pready(gg), (t >> 1) & 1)) return false;
       if (!wait_all(vfull(s), (t / VS) & 1)) return false;
       tc_fence_after();
-      const uint32_t vb = (sbase + Cfg::kOffV + s * Cfg::kKV) >> 4;
+      const uint32_t vb = (sbase + Cfg::kOffV + s * Cfg::kVS) >> 4;
       const uint32_t pb = (sbase + Cfg::kOffP + gg * Cfg::kP) >> 4;
       if (leader) {
 #pragma unroll
         for (int kp = 0; kp < 8; ++kp)
-          tc_mma(tmem + 64 + 32 * gg, with_addr(dVmn, vb + kp * 128),
+          tc_mma(tmem + 2 * kCol + kCol * gg, with_addr(dVmn, vb + kp * 128),
                  with_addr(dSw, pb + (kp >> 2) * (NQP * 8) + (kp & 3) * 2), idPV, t >= 2 || kp > 0);
         tc_commit(pvdone(gg));
         tc_commit(vfree(s));
@@ -364,8 +400,8 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t kb = (sbase + s * Cfg::kKV) >> 4;
       if (leader) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc_mma(tmem + 32 * gg, with_addr(dSw, kb + (ks >> 2) * 1024 + (ks & 3) * 2),
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma(tmem + kCol * gg, with_addr(dSw, kb + (ks >> 2) * 1024 + (ks & 3) * 2),
                  with_addr(dSw, qb + (ks >> 2) * (NQP * 8) + (ks & 3) * 2), idS, ks > 0);
         tc_commit(sfull(gg));
         tc_commit(kfree(s));
@@ -385,17 +421,26 @@ __global__ void __launch_bounds__(384, 1)
     const int q4 = warp & 3;                  // tensor-memory lane quarter of this warp
     const int i = 32 * q4 + lane;             // tile position / head dimension owned
     const uint32_t tl = tmem + (uint32_t(32 * q4) << 16);
-    const uint32_t s_col = 32 * grp, o_col = 64 + 32 * grp;
-    float m[NQC], ls[NQC];
+    const uint32_t s_col = kCol * grp, o_col = 2 * kCol + kCol * grp;
+    // Running maxima per column: registers, or (wide tiles) the group's mrun row,
+    // read by broadcast; row sums per column and thread, unless V's ones row
+    // makes the PV MMA accumulate them.
+    constexpr bool kSmemMax = Cfg::kSmemMax;
+    float m[kSmemMax ? 1 : NQC], ls[Cfg::kOnesRow ? 1 : NQC];
 #pragma unroll
     for (int n = 0; n < NQC; ++n) {
-      m[n] = kEmptyMax;
-      ls[n] = 0.f;
+      if constexpr (!kSmemMax) m[n] = kEmptyMax;
+      if constexpr (!Cfg::kOnesRow) ls[n] = 0.f;
     }
-    uint32_t colbits = 0;
+    float* mg = mrun + grp * NQC;
+    if constexpr (kSmemMax) {
+      if (i < NQC) mg[i] = kEmptyMax;
+      named_bar(1 + grp, 128);
+    }
+    uint64_t colbits = 0;
 #pragma unroll
     for (int n = 0; n < NQC; ++n)
-      if (n < p.nq) colbits |= 1u << n;
+      if (n < p.nq) colbits |= 1ull << n;
     float* srow = CAPTURE ? p.scores + size_t(unit) * p.score_stride : nullptr;
     int Lcap = L;
     if (CAPTURE && L > p.score_stride) {
@@ -446,10 +491,10 @@ __global__ void __launch_bounds__(384, 1)
       if (okt && lpos > last_valid) {
         // a cache slot past the window: zero its V row so 0 * garbage cannot be NaN
         okt = mbar_wait_bounded(vfull(s), (t / VS) & 1);
-        uint8_t* vrow = smem + Cfg::kOffV + s * Cfg::kKV + i * 128;
+        uint8_t* vrow = smem + Cfg::kOffV + s * Cfg::kVS + i * 128;
         if (okt) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < Cfg::kHalves; ++h)
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc)
               *reinterpret_cast<uint4*>(vrow + h * 16384 + ((cc ^ (i & 7)) << 4)) =
@@ -461,10 +506,13 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int n = 0; n < NQC; ++n) {
         float v = x[n] * p.scale_log2;
-        if (!live || !((colbits >> n) & 1u)) v = -INFINITY;
+        if (!live || !((colbits >> n) & 1ull)) v = -INFINITY;
         if (tail && pos > L + tlim[n]) v = -INFINITY;
         x[n] = v;
-        need |= v > m[n] + kRescaleSlack;
+        if constexpr (kSmemMax)
+          need |= v > mg[n] + kRescaleSlack;
+        else
+          need |= v > m[n] + kRescaleSlack;
       }
       const int wvote = (__any_sync(0xffffffffu, need) ? 1 : 0) | (__any_sync(0xffffffffu, !okt) ? 2 : 0);
       if (lane == 0) votes[grp * 4 + q4] = wvote;
@@ -487,38 +535,71 @@ __global__ void __launch_bounds__(384, 1)
           if (lane == 0) colmax[(grp * 4 + q4) * NQC + n] = v;
         }
         named_bar(1 + grp, 128);
-        float f[NQC];
+        const float* cm = colmax + grp * 4 * NQC;
+        auto new_max = [&](int n, float mold) {
+          return fmaxf(mold, fmaxf(fmaxf(cm[n], cm[NQC + n]), fmaxf(cm[2 * NQC + n], cm[3 * NQC + n])));
+        };
+        if constexpr (!kSmemMax) {
+          float f[NQC];
 #pragma unroll
-        for (int n = 0; n < NQC; ++n) {
-          const float* cm = colmax + grp * 4 * NQC;
-          const float mx = fmaxf(fmaxf(cm[n], cm[NQC + n]), fmaxf(cm[2 * NQC + n], cm[3 * NQC + n]));
-          const float mn = fmaxf(m[n], mx);
-          f[n] = ex2(m[n] - mn);
-          m[n] = mn;
-          ls[n] *= f[n];
-        }
-        if (k > 0 && pv_ok) {
-          // O^T row i of this group, columns scaled by f
+          for (int n = 0; n < NQC; ++n) {
+            const float mn = new_max(n, m[n]);
+            f[n] = ex2(m[n] - mn);
+            m[n] = mn;
+            if constexpr (!Cfg::kOnesRow) ls[n] *= f[n];
+          }
+          if (k > 0 && pv_ok) {
+            // O^T row i of this group, columns scaled by f
+#pragma unroll
+            for (int c = 0; c < NQC / 8; ++c) {
+              float v8[8];
+              tmem_ld8(tl + o_col + 8 * c, v8);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v8[e] *= f[8 * c + e];
+              tmem_st8(tl + o_col + 8 * c, v8);
+            }
+            tmem_st_wait();
+          }
+          named_bar(1 + grp, 128);   // colmax is rewritten at the next rescale
+        } else {
+          // factors recomputed per 8-column chunk from the old maxima in mrun
 #pragma unroll
           for (int c = 0; c < NQC / 8; ++c) {
-            float v8[8];
-            tmem_ld8(tl + o_col + 8 * c, v8);
-            tmem_ld_wait();
+            float f8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v8[e] *= f[8 * c + e];
-            tmem_st8(tl + o_col + 8 * c, v8);
+            for (int e = 0; e < 8; ++e) {
+              const float mold = mg[8 * c + e];
+              f8[e] = ex2(mold - new_max(8 * c + e, mold));
+              if constexpr (!Cfg::kOnesRow) ls[8 * c + e] *= f8[e];
+            }
+            if (k > 0 && pv_ok) {
+              float v8[8];
+              tmem_ld8(tl + o_col + 8 * c, v8);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v8[e] *= f8[e];
+              tmem_st8(tl + o_col + 8 * c, v8);
+            }
           }
-          tmem_st_wait();
+          if (k > 0 && pv_ok) tmem_st_wait();
+          named_bar(1 + grp, 128);   // every thread has read the old maxima
+          if (i < NQC) mg[i] = new_max(i, mg[i]);
+          named_bar(1 + grp, 128);   // new maxima visible; colmax free again
         }
-        named_bar(1 + grp, 128);   // colmax is rewritten at the next rescale
       }
       // P^T operand, K-major with the 128-byte swizzle: element (n, i) at
       // (i / 64) * NQP * 128 + n * 128 + (((i % 64) / 8) ^ (n % 8)) * 16 + (i % 8) * 2.
       uint8_t* pbuf = smem + Cfg::kOffP + grp * Cfg::kP + (i >> 6) * (NQP * 128) + (i & 7) * 2;
 #pragma unroll
       for (int n = 0; n < NQC; ++n) {
-        const float pv = ex2(x[n] - m[n]);
-        ls[n] += pv;
+        float mn;
+        if constexpr (kSmemMax)
+          mn = mg[n];
+        else
+          mn = m[n];
+        const float pv = ex2(x[n] - mn);
+        if constexpr (!Cfg::kOnesRow) ls[n] += pv;
         *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((((i & 63) >> 3) ^ (n & 7)) << 4)) =
             __float2bfloat16_rn(pv);
       }
@@ -536,12 +617,14 @@ __global__ void __launch_bounds__(384, 1)
     // Each group's (m, l, O^T) is a partial state of its own, merged together
     // with the splits' states, so no group waits on the other's arithmetic.
     // Row sums over the group's 128 positions:
+    if constexpr (!Cfg::kOnesRow) {
 #pragma unroll
-    for (int n = 0; n < NQC; ++n) {
-      float v = ls[n];
+      for (int n = 0; n < NQC; ++n) {
+        float v = ls[n];
 #pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
-      if (lane == 0) colsum[(grp * 4 + q4) * NQC + n] = v;
+        for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+        if (lane == 0) colsum[(grp * 4 + q4) * NQC + n] = v;
+      }
     }
     // this thread's O^T row (head dimension i), unnormalised
 #pragma unroll
@@ -556,20 +639,32 @@ __global__ void __launch_bounds__(384, 1)
       }
       tmem_ld_wait();
     }
+    if constexpr (Cfg::kOnesRow) {
+      // O^T row 64 accumulated the column sums of P (V's ones row)
+      if (i == 64) {
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) colsum[grp * 4 * NQC + n] = o[n];
+      }
+    }
     named_bar(1 + grp, 128);
     if (i < NQC) {
       const float* cs = colsum + grp * 4 * NQC;
-      if (mytiles > 0) Lg = cs[i] + cs[NQC + i] + cs[2 * NQC + i] + cs[3 * NQC + i];
+      if (mytiles > 0)
+        Lg = Cfg::kOnesRow ? cs[i] : cs[i] + cs[NQC + i] + cs[2 * NQC + i] + cs[3 * NQC + i];
+      if constexpr (kSmemMax) {
+        Mg = mg[i];
+      } else {
 #pragma unroll
-      for (int n = 0; n < NQC; ++n)
-        if (n == i) Mg = m[n];
+        for (int n = 0; n < NQC; ++n)
+          if (n == i) Mg = m[n];
+      }
     }
     if (!on_chip) {
       // partial 2 * split + grp of the unit's 2 * num_splits
       const size_t part = (size_t(unit) * p.num_splits + split) * 2 + grp;
 #pragma unroll
       for (int n = 0; n < NQC; ++n)
-        if (n < p.nq) p.part_o[(part * p.nq + n) * D + i] = o[n];
+        if (n < p.nq && i < D) p.part_o[(part * p.nq + n) * D + i] = o[n];
       if (i < p.nq) {
         p.part_ml[(part * p.nq + i) * 2 + 0] = Mg;
         p.part_ml[(part * p.nq + i) * 2 + 1] = Lg;
@@ -606,7 +701,8 @@ __global__ void __launch_bounds__(384, 1)
     static_assert(2 * (NQC + kMaxVerifyCluster) * RS * 4 <= KS * Cfg::kKV, "receive area");
     static_assert(2 * kMaxVerifyCluster <= 32, "one lane per state in the weight pass");
     cg::cluster_group cluster = cg::this_cluster();
-    const int S = p.num_splits, r = (int)cluster.block_rank();
+    const int S = p.cluster_merge ? p.cluster_size : 1, r = (int)cluster.block_rank();
+    const int C = p.num_splits / S, c = split / S;   // clusters of the unit, this one's index
     const float* recv = reinterpret_cast<const float*>(smem);
     if (warp >= 2 && warp <= 9) {
       const int grp = (warp - 2) >> 2, i = 32 * (warp & 3) + lane;
@@ -614,7 +710,7 @@ __global__ void __launch_bounds__(384, 1)
       int owner = 0, slot = 0;
 #pragma unroll
       for (int n = 0; n < NQC; ++n) {
-        if (n < p.nq)
+        if (n < p.nq && i < D)
           st_cluster_f32(cluster_map(sbase + 4 * ((slot * 2 * S + q) * RS + i), owner), o[n]);
         if (++owner == S) {
           owner = 0;
@@ -630,8 +726,13 @@ __global__ void __launch_bounds__(384, 1)
     cluster_sync_all();
     const int nown = r < p.nq ? (p.nq - r + S - 1) / S : 0;
     // Weights 2^(m_q - M) / sum_q' 2^(m_q' - M) l_q' of the 2S states of each
-    // owned row (one warp per row, lane q), into the free V ring ...
+    // owned row (one warp per row, lane q), into the free V ring, with the
+    // row's cluster-level maximum M and sum (used when C > 1) ...
+    // (nown <= NQC <= 64 rows, 2S <= 32 states, C <= 32 clusters)
+    static_assert((64 * 2 * kMaxVerifyCluster + 2 * 64 + 64 * 32) * 4 <= VS * Cfg::kVS,
+                  "merge weights fit the V ring");
     float* wts = reinterpret_cast<float*>(smem + Cfg::kOffV);   // [nown][2S]
+    float* rowml = wts + 64 * 2 * kMaxVerifyCluster;           // [nown][2]
     for (int k = warp; k < nown; k += Cfg::kThreads / 32) {
       const float* st = recv + k * 2 * S * RS;
       const bool has = lane < 2 * S;
@@ -645,6 +746,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int o2 = 16; o2 > 0; o2 >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o2);
       if (has) wts[k * 2 * S + lane] = Lsum > 0.f ? f / Lsum : 0.f;
+      if (lane == 0) {
+        rowml[2 * k] = M;
+        rowml[2 * k + 1] = Lsum;
+      }
     }
     __syncthreads();
     // ... then four output elements per thread: sum_q w_q O_q[d .. d + 3]
@@ -662,12 +767,72 @@ __global__ void __launch_bounds__(384, 1)
         acc.z += wq * v.z;
         acc.w += wq * v.w;
       }
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(out_row(r + k * S) + d) = pk;
+      if (C == 1) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out_row(r + k * S) + d) = pk;
+      } else {
+        // this cluster's normalised row, merged across the unit's clusters below
+        const size_t row = (size_t(unit) * C + c) * p.nq + (r + k * S);
+        *reinterpret_cast<float4*>(p.part_o + row * D + d) = acc;
+      }
+    }
+    if (C > 1) {
+      // Cross-cluster merge through the workspace, per owner rank: rank r of
+      // every cluster of the unit writes its rows' (o_c, M_c, L_c), takes the
+      // ticket of (unit, r), and the last to arrive combines them:
+      // out = sum_c F_c o_c / sum_c F_c with F_c = 2^(M_c - max M) L_c.
+      for (int k = tid; k < nown; k += Cfg::kThreads) {
+        const size_t row = (size_t(unit) * C + c) * p.nq + (r + k * S);
+        p.part_ml[2 * row] = rowml[2 * k];
+        p.part_ml[2 * row + 1] = rowml[2 * k + 1];
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) *flag = atomicAdd(&p.tickets[unit * S + r], 1) == C - 1;
+      __syncthreads();
+      if (*flag) {
+        __threadfence();
+        float* w2 = rowml + 2 * 64;   // [nown][C]
+        for (int k = warp; k < nown; k += Cfg::kThreads / 32) {
+          const bool has = lane < C;
+          const size_t row = (size_t(unit) * C + lane) * p.nq + (r + k * S);
+          const float m = has ? __ldcg(&p.part_ml[2 * row]) : kEmptyMax;
+          const float l = has ? __ldcg(&p.part_ml[2 * row + 1]) : 0.f;
+          float M = m;
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+          const float F = has ? ex2(m - M) * l : 0.f;
+          float Fs = F;
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) Fs += __shfl_xor_sync(0xffffffffu, Fs, o2);
+          if (has) w2[k * C + lane] = Fs > 0.f ? F / Fs : 0.f;
+        }
+        __syncthreads();
+        for (int e = tid; e < nown * (D / 4); e += Cfg::kThreads) {
+          const int k = e / (D / 4), d = 4 * (e - k * (D / 4));
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < C; ++q) {
+            const size_t row = (size_t(unit) * C + q) * p.nq + (r + k * S);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + row * D + d));
+            const float wq = w2[k * C + q];
+            acc.x += wq * v.x;
+            acc.y += wq * v.y;
+            acc.z += wq * v.z;
+            acc.w += wq * v.w;
+          }
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(out_row(r + k * S) + d) = pk;
+        }
+        if (tid == 0) p.tickets[unit * S + r] = 0;
+      }
     }
   } else {
     SplitWorkspace ws{p.tickets, p.part_ml, p.part_o};
@@ -676,28 +841,28 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int NQP, int NQC, bool CAP>
+template <int D, int NQP, int NQC, bool CAP>
 static cudaError_t configure_tc() {
-  using Cfg = TcCfg<NQP, NQC>;
+  using Cfg = TcCfg<D, NQP, NQC>;
   static std::atomic<uint32_t> configured{0};
   return once_per_device(configured, [] {
-    cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<NQP, NQC, CAP>,
+    cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<D, NQP, NQC, CAP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(verify_tc_kernel<NQP, NQC, CAP>,
+    return cudaFuncSetAttribute(verify_tc_kernel<D, NQP, NQC, CAP>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
 }
 
 // Launch (launch = true) or, with launch = false, the number of clusters of
-// p.num_splits CTAs that can be resident at once (into *clusters).
-template <int NQP, int NQC, bool CAP>
+// p.cluster_size CTAs that can be resident at once (into *clusters).
+template <int D, int NQP, int NQC, bool CAP>
 static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const VerifyParams& p, int batch, cudaStream_t stream, bool launch,
                              int* clusters) {
-  using Cfg = TcCfg<NQP, NQC>;
-  cudaError_t e = configure_tc<NQP, NQC, CAP>();
+  using Cfg = TcCfg<D, NQP, NQC>;
+  cudaError_t e = configure_tc<D, NQP, NQC, CAP>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits, p.hkv, batch);
@@ -706,44 +871,64 @@ static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cluster_merge ? p.num_splits : 1;
+  attr[0].val.clusterDim.x = p.cluster_merge ? p.cluster_size : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = launch ? 2 : 1;
-  if (!launch) return cudaOccupancyMaxActiveClusters(clusters, verify_tc_kernel<NQP, NQC, CAP>, &cfg);
-  return cudaLaunchKernelEx(&cfg, verify_tc_kernel<NQP, NQC, CAP>, kmap, vmap, p);
+  if (!launch)
+    return cudaOccupancyMaxActiveClusters(clusters, verify_tc_kernel<D, NQP, NQC, CAP>, &cfg);
+  return cudaLaunchKernelEx(&cfg, verify_tc_kernel<D, NQP, NQC, CAP>, kmap, vmap, p);
 }
 
-template <bool CAP>
+// Column tiles of 8: the processed columns NQC and the MMA width NQP.
+template <int D, bool CAP>
 static cudaError_t launch_tc_cols(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                   const VerifyParams& p, int ncols, int batch, cudaStream_t s,
                                   bool launch, int* clusters) {
   switch ((ncols + 7) / 8) {
-    case 1: return launch_tc<16, 8, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    case 2: return launch_tc<16, 16, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    case 3: return launch_tc<32, 24, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    case 4: return launch_tc<32, 32, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    default: return cudaErrorInvalidValue;
+    case 1: return launch_tc<D, 16, 8, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    case 2: return launch_tc<D, 16, 16, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    case 3: return launch_tc<D, 32, 24, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    case 4: return launch_tc<D, 32, 32, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    case 5: return launch_tc<D, 64, 40, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+    default: break;
   }
+  if constexpr (D == 64) {
+    switch ((ncols + 7) / 8) {
+      case 6: return launch_tc<D, 64, 48, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+      case 7: return launch_tc<D, 64, 56, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+      case 8: return launch_tc<D, 64, 64, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+      default: break;
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             const VerifyParams& p, int ncols, bool capture, int batch,
-                             cudaStream_t stream) {
-  return capture ? launch_tc_cols<true>(kmap, vmap, p, ncols, batch, stream, true, nullptr)
-                 : launch_tc_cols<false>(kmap, vmap, p, ncols, batch, stream, true, nullptr);
+#define VEGAS_CAT2(a, b) a##b
+#define VEGAS_CAT(a, b) VEGAS_CAT2(a, b)
+
+cudaError_t VEGAS_CAT(launch_verify_tc_d, VEGAS_TC_D)(const CUtensorMap& kmap,
+                                                     const CUtensorMap& vmap,
+                                                     const VerifyParams& p, int ncols,
+                                                     bool capture, int batch,
+                                                     cudaStream_t stream) {
+  constexpr int D = VEGAS_TC_D;
+  return capture ? launch_tc_cols<D, true>(kmap, vmap, p, ncols, batch, stream, true, nullptr)
+                 : launch_tc_cols<D, false>(kmap, vmap, p, ncols, batch, stream, true, nullptr);
 }
 
-int verify_tc_max_active_clusters(int ncols, bool capture, int cluster) {
+int VEGAS_CAT(verify_tc_max_active_clusters_d, VEGAS_TC_D)(int ncols, bool capture,
+                                                          int cluster) {
+  constexpr int D = VEGAS_TC_D;
   if (cluster < 1 || cluster > kMaxVerifyCluster) return 0;
   constexpr int kDevices = 32;
   // [device][capture][column tiles][cluster]: 0 unknown, -1 none, else the count
-  static std::atomic<int> cache[kDevices][2][5][kMaxVerifyCluster + 1];
+  static std::atomic<int> cache[kDevices][2][9][kMaxVerifyCluster + 1];
   const int ct = (ncols + 7) / 8;
-  if (ct < 1 || ct > 4) return 0;
+  if (ct < 1 || ct > verify_tc_max_columns(D) / 8) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return 0;
   std::atomic<int>& slot = cache[dev][capture ? 1 : 0][ct][cluster];
@@ -752,11 +937,12 @@ int verify_tc_max_active_clusters(int ncols, bool capture, int cluster) {
     VerifyParams p{};
     p.hkv = 1;
     p.num_splits = cluster;
+    p.cluster_size = cluster;
     p.cluster_merge = 1;
     CUtensorMap none{};
     int n = 0;
-    cudaError_t e = capture ? launch_tc_cols<true>(none, none, p, ncols, 1, 0, false, &n)
-                            : launch_tc_cols<false>(none, none, p, ncols, 1, 0, false, &n);
+    cudaError_t e = capture ? launch_tc_cols<D, true>(none, none, p, ncols, 1, 0, false, &n)
+                            : launch_tc_cols<D, false>(none, none, p, ncols, 1, 0, false, &n);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       n = 0;

@@ -48,8 +48,9 @@ def test_k_larger_than_prefix_sets_device_fault():
 
 
 def test_small_workspace_is_rejected_on_the_host():
-    # head_dim 64: the mma.sync kernel merges its splits through the workspace
-    c = Case(configs.GPTOSS_20B_B4_128K.with_(batch=1, ctx_lo=4000, ctx_hi=4000))
+    # 44 query rows at head_dim 128: the mma.sync kernel merges its splits
+    # through the workspace
+    c = Case(configs.QWEN3_8B_B1_32K.with_(gamma=10, ctx_lo=4000, ctx_hi=4000))
     need = vg.vegas_verify_workspace_size(c.kv, 1, c.w.gamma)
     assert need > 0
     ws = torch.zeros(need // 2, dtype=torch.uint8, device="cuda")

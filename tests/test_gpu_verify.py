@@ -122,8 +122,9 @@ def test_repeat_calls_are_deterministic():
 
 
 def test_cluster_merged_shape_needs_no_workspace():
-    # 8 (sequence, KV head) units at head_dim 128: the splits merge on chip
-    c = Case(C2.with_(ctx_lo=5000, ctx_hi=5000), device_gen=True)
+    # 64 (sequence, KV head) units at head_dim 128: one 2-CTA cluster per unit,
+    # whose splits merge on chip
+    c = Case(C3.with_(batch=8, ctx_lo=2000, ctx_hi=2000), device_gen=True)
     w = c.w
     assert vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma) == 0
     ref_out, ref_scores = c.verify()
@@ -133,7 +134,27 @@ def test_cluster_merged_shape_needs_no_workspace():
                                  0, w.gamma, c.scale, None, 0)
     vg.vegas_read_device_status()
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
-    assert torch.equal(scores[..., :5000], ref_scores[..., :5000])
+    assert torch.equal(scores[..., :2000], ref_scores[..., :2000])
+
+
+def test_several_clusters_per_unit_merge_through_the_workspace():
+    """Few units (8 at batch 1): each unit's splits form several clusters, merged
+    on chip within a cluster and through a few workspace rows across clusters;
+    repeated calls leave the tickets at zero and give identical results."""
+    c = Case(C2.with_(ctx_lo=5000, ctx_hi=5000))
+    w = c.w
+    nb = vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma)
+    assert nb > 0
+    ref_out, ref_scores = _check_case(c)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")       # one workspace, reused
+    for _ in range(2):
+        out = torch.empty_like(c.qv)
+        scores = torch.full_like(ref_scores, float("nan"))
+        vg.vegas_verify_attn_capture(c.kv, c.qv, out, scores, c.stride, c.lens_t, w.batch,
+                                     w.gamma, 0, w.gamma, c.scale, ws, nb)
+        vg.vegas_read_device_status()
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(scores[..., :5000], ref_scores[..., :5000])
 
 
 @pytest.mark.parametrize("name", ["tiny", "qwen_b1_ragged", "gptoss_b2", "qwen_b3_var"])

@@ -31,12 +31,13 @@ def _noalloc(c: Case):
     return out, scores
 
 
-# Shapes whose split-KV merge goes through the scratch (the mma.sync kernel:
-# head_dim 64, or more than 32 query columns at head_dim 128).
+# Shapes whose split-KV merge goes through the scratch: 44 query rows at
+# head_dim 128 (the mma.sync kernel), and 160 (sequence, KV head) units (more
+# than the SMs: the tcgen05 kernel's last-arriving-CTA merge).
 @pytest.mark.parametrize("w", [
-    configs.GPTOSS_20B_B4_128K.with_(batch=1, ctx_lo=20000, ctx_hi=20000),
-    configs.QWEN3_8B_B8_48K_64K.with_(batch=3, ctx_lo=3000, ctx_hi=9000, gamma=8),
-], ids=["gptoss_b1", "qwen_b3_gamma8"])
+    configs.QWEN3_8B_B8_48K_64K.with_(batch=3, ctx_lo=3000, ctx_hi=9000, gamma=10),
+    configs.QWEN3_8B_B8_48K_64K.with_(batch=20, ctx_lo=250, ctx_hi=300),
+], ids=["qwen_b3_gamma10", "qwen_b20_160_units"])
 def test_noalloc_matches_workspace_entry_point_twice(w):
     c = Case(w, device_gen=True)
     assert 0 < vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma) <= \
