@@ -124,29 +124,39 @@ vegas_status_t verify_two_rows(const vegas_paged_kv_t* kv, const void* q, void* 
 
 // Largest 8-row query tile count per head_dim (d=128: 48 rows, d=64: 64 rows).
 inline int verify_max_ntiles(int head_dim) { return head_dim == 128 ? 6 : 8; }
-// tcgen05 verify kernel (head_dim 128 with at most 40 query columns incl.
-// capture, head_dim 64 with at most 64), streaming 8-page tiles.
-inline int verify_tc_max_columns(int head_dim) { return head_dim == 128 ? 40 : 64; }
+// tcgen05 verify kernel.  Its softmax handles the nq = (gamma+1)*G query
+// columns rounded up to 8 (at most 40 at head_dim 128, 64 at head_dim 64); with
+// capture, the two summed-query columns follow them in the MMA (N = 16, 32 or
+// 64 columns in all).
+inline int verify_tc_mma_columns(int nq, bool capture) {
+  const int need = (nq + 7) / 8 * 8 + (capture ? 2 : 0);
+  return need <= 16 ? 16 : need <= 32 ? 32 : need <= 64 ? 64 : 0;
+}
+inline bool verify_tc_supported(int head_dim, int nq, bool capture) {
+  const int nqc = (nq + 7) / 8 * 8;
+  return nq >= 1 && verify_tc_mma_columns(nq, capture) > 0 &&
+         nqc <= (head_dim == 128 ? 40 : 64);
+}
 constexpr int kTcPagesPerTile = 8;
 constexpr int kMaxVerifyCluster = 16;   // splits merged on chip (non-portable cluster size)
 cudaError_t launch_verify_tc_d64(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const VerifyParams& p, int ncols, bool capture, int batch,
+                                 const VerifyParams& p, bool capture, int batch,
                                  cudaStream_t stream);
 cudaError_t launch_verify_tc_d128(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                  const VerifyParams& p, int ncols, bool capture, int batch,
+                                  const VerifyParams& p, bool capture, int batch,
                                   cudaStream_t stream);
 inline cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                    const VerifyParams& p, int head_dim, int ncols, bool capture,
-                                    int batch, cudaStream_t stream) {
-  return head_dim == 64 ? launch_verify_tc_d64(kmap, vmap, p, ncols, capture, batch, stream)
-                        : launch_verify_tc_d128(kmap, vmap, p, ncols, capture, batch, stream);
+                                    const VerifyParams& p, int head_dim, bool capture, int batch,
+                                    cudaStream_t stream) {
+  return head_dim == 64 ? launch_verify_tc_d64(kmap, vmap, p, capture, batch, stream)
+                        : launch_verify_tc_d128(kmap, vmap, p, capture, batch, stream);
 }
 // Clusters of `cluster` CTAs of the tcgen05 kernel resident at once (0: none / error).
-int verify_tc_max_active_clusters_d64(int ncols, bool capture, int cluster);
-int verify_tc_max_active_clusters_d128(int ncols, bool capture, int cluster);
-inline int verify_tc_max_active_clusters(int head_dim, int ncols, bool capture, int cluster) {
-  return head_dim == 64 ? verify_tc_max_active_clusters_d64(ncols, capture, cluster)
-                        : verify_tc_max_active_clusters_d128(ncols, capture, cluster);
+int verify_tc_max_active_clusters_d64(int nq, bool capture, int cluster);
+int verify_tc_max_active_clusters_d128(int nq, bool capture, int cluster);
+inline int verify_tc_max_active_clusters(int head_dim, int nq, bool capture, int cluster) {
+  return head_dim == 64 ? verify_tc_max_active_clusters_d64(nq, capture, cluster)
+                        : verify_tc_max_active_clusters_d128(nq, capture, cluster);
 }
 template <int D, bool CAP>
 cudaError_t launch_verify_t(const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -160,7 +160,7 @@ int verify_splits(int units, int max_pages, int sms) {
 
 struct VerifyPlan {
   int nq, ncols, ntiles, splits, pages_per_split;
-  bool tc;        // tcgen05 kernel (head_dim 128, <= 32 columns) instead of the mma.sync one
+  bool tc;        // tcgen05 kernel instead of the mma.sync one (verify_tc_supported)
   bool cluster;   // tcgen05 kernel with a unit's splits in clusters merging on chip
   int cluster_size;   // CTAs per cluster; splits / cluster_size clusters per unit
   bool needs_ws;      // partials or tickets go through the workspace
@@ -178,7 +178,7 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
   pl.nq = (gamma + 1) * G;
   pl.ncols = verify_columns(pl.nq, capture);
   pl.ntiles = (pl.ncols + 7) / 8;
-  pl.tc = pl.ncols <= vegas::verify_tc_max_columns(kv->head_dim);
+  pl.tc = vegas::verify_tc_supported(kv->head_dim, pl.nq, capture);
   const int units = std::max(1, batch * kv->num_kv_heads);
   if (pl.tc && units < sms && with_device) {
     // C clusters of S CTAs per unit, every CTA resident (one wave), >= one tile
@@ -186,10 +186,11 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
     // cluster's splits merge through distributed shared memory, the clusters of
     // a unit through a few rows of the workspace.
     const int max_splits = std::max(1, kv->max_pages_per_seq / vegas::kTcPagesPerTile);
-    int bestS = 0, bestC = 0;
+    int bestS = 0, bestC = 0, oneS = 0;
     for (int S = std::min(vegas::kMaxVerifyCluster, sms / units); S >= 2; --S) {
       const int resident =
-          vegas::verify_tc_max_active_clusters(kv->head_dim, pl.ncols, capture, S);
+          vegas::verify_tc_max_active_clusters(kv->head_dim, pl.nq, capture, S);
+      if (!oneS && S <= max_splits && resident >= units) oneS = S;
       // (the cross-cluster merge takes one lane per cluster: C <= 32)
       int C = std::min(std::min(sms / (units * S), max_splits / S), 32);
       while (C > 0 && resident < units * C) --C;
@@ -197,6 +198,13 @@ VerifyPlan plan_verify(const vegas_paged_kv_t* kv, int batch, int gamma, int sms
         bestS = S;
         bestC = C;
       }
+    }
+    // One cluster per unit when it already covers 60% of the SMs: more CTAs
+    // measured no faster there (the stream is not what limits a launch), and
+    // it needs no workspace.
+    if (oneS > 1 && 10 * oneS * units >= 6 * sms) {
+      bestS = oneS;
+      bestC = 1;
     }
     if (bestS > 1) {
       // split s takes pages [s * max_pages / n, (s + 1) * max_pages / n): >= 8 each
@@ -482,7 +490,7 @@ vegas_status_t verify_impl(const vegas_paged_kv_t* kv, const void* q, void* out,
     if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
   }
   cudaError_t e =
-      pl.tc ? vegas::launch_verify_tc(km, vm, p, kv->head_dim, pl.ncols, scores != nullptr, batch,
+      pl.tc ? vegas::launch_verify_tc(km, vm, p, kv->head_dim, scores != nullptr, batch,
                                       static_cast<cudaStream_t>(stream))
             : launch_verify_any(km, vm, p, kv->head_dim, pl.ntiles, scores != nullptr, batch,
                                 static_cast<cudaStream_t>(stream));

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(384, 1)
   constexpr int kCol = Cfg::kCol;
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(NQP == 16 || NQP == 32 || NQP == 64, "MMA N");
-  static_assert(NQC % 8 == 0 && NQC <= NQP, "processed columns");
+  static_assert(NQC % 8 == 0 && NQC + (CAPTURE ? 2 : 0) <= NQP, "processed columns");
   static_assert(Cfg::kSmem <= 227 * 1024, "shared memory");
 
   griddep_launch_dependents();
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(384, 1)
   const int npages = (L + T + 15) / 16;
   const int pend = min(pnext, npages);
   const int ntiles = pend > pbeg ? (pend - pbeg + 7) / 8 : 0;
-  const int cap0 = (p.nq + 1) & ~1;
+  constexpr int cap0 = NQC;   // the summed captured query: MMA columns NQC and NQC + 1
   const int last_valid = L + p.gamma;
 
   __syncthreads();   // barriers initialised before anyone waits on them
@@ -437,10 +437,8 @@ __global__ void __launch_bounds__(384, 1)
       if (i < NQC) mg[i] = kEmptyMax;
       named_bar(1 + grp, 128);
     }
-    uint64_t colbits = 0;
-#pragma unroll
-    for (int n = 0; n < NQC; ++n)
-      if (n < p.nq) colbits |= 1ull << n;
+    // Columns nq .. NQC - 1 multiply zero query rows: their logits are 0, they
+    // never raise a maximum after the first tile and nothing reads their output.
     float* srow = CAPTURE ? p.scores + size_t(unit) * p.score_stride : nullptr;
     int Lcap = L;
     if (CAPTURE && L > p.score_stride) {
@@ -455,6 +453,7 @@ __global__ void __launch_bounds__(384, 1)
       bool okt = ok && mbar_wait_bounded(sfull(grp), k & 1);
       tc_fence_after();
       float x[NQC];
+      float cx[2] = {0.f, 0.f};   // the two capture columns
 #pragma unroll
       for (int n = 0; n < NQC; ++n) x[n] = 0.f;
       if (okt) {
@@ -465,6 +464,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[8 * c + e] = v8[e];
         }
+        if constexpr (CAPTURE) tmem_ld2(tl + s_col + cap0, cx);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(sread(grp));
@@ -472,13 +472,7 @@ __global__ void __launch_bounds__(384, 1)
       const int page = pbeg + 8 * t + (i >> 4);
       const bool live = page < pend;
       const int pos = page * 16 + (i & 15);
-      if (CAPTURE && okt && live && pos < Lcap) {
-        float c = 0.f;
-#pragma unroll
-        for (int n = 0; n < NQC; ++n)
-          if (n == cap0 || n == cap0 + 1) c += x[n];
-        srow[pos] = c * p.scale;
-      }
+      if (CAPTURE && okt && live && pos < Lcap) srow[pos] = (cx[0] + cx[1]) * p.scale;
       if (!CAPTURE && p.raw && okt && live && pos < min(L, p.raw_stride)) {
         // the pages' way: every captured row's logit of every head goes to memory
 #pragma unroll
@@ -501,18 +495,24 @@ __global__ void __launch_bounds__(384, 1)
                   make_uint4(0, 0, 0, 0);
         }
       }
-      const bool tail = pos > L;
+      // logits in log2 units; positions past the range, and window positions a
+      // row may not see yet (pos > L + t), are masked
+      const float sl2 = live ? p.scale_log2 : 0.f;
+      const float bias = live ? 0.f : -INFINITY;
+#pragma unroll
+      for (int n = 0; n < NQC; ++n) x[n] = fmaf(x[n], sl2, bias);
+      if (pos > L) {
+#pragma unroll
+        for (int n = 0; n < NQC; ++n)
+          if (pos > L + tlim[n]) x[n] = -INFINITY;
+      }
       bool need = false;
 #pragma unroll
       for (int n = 0; n < NQC; ++n) {
-        float v = x[n] * p.scale_log2;
-        if (!live || !((colbits >> n) & 1ull)) v = -INFINITY;
-        if (tail && pos > L + tlim[n]) v = -INFINITY;
-        x[n] = v;
         if constexpr (kSmemMax)
-          need |= v > mg[n] + kRescaleSlack;
+          need |= x[n] > mg[n] + kRescaleSlack;
         else
-          need |= v > m[n] + kRescaleSlack;
+          need |= x[n] > m[n] + kRescaleSlack;
       }
       const int wvote = (__any_sync(0xffffffffu, need) ? 1 : 0) | (__any_sync(0xffffffffu, !okt) ? 2 : 0);
       if (lane == 0) votes[grp * 4 + q4] = wvote;
@@ -590,7 +590,9 @@ __global__ void __launch_bounds__(384, 1)
       }
       // P^T operand, K-major with the 128-byte swizzle: element (n, i) at
       // (i / 64) * NQP * 128 + n * 128 + (((i % 64) / 8) ^ (n % 8)) * 16 + (i % 8) * 2.
+      // (row n, chunk c ^ (n % 8)): eight chunk offsets cover every n
       uint8_t* pbuf = smem + Cfg::kOffP + grp * Cfg::kP + (i >> 6) * (NQP * 128) + (i & 7) * 2;
+      const int ci = (i & 63) >> 3;
 #pragma unroll
       for (int n = 0; n < NQC; ++n) {
         float mn;
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(384, 1)
           mn = m[n];
         const float pv = ex2(x[n] - mn);
         if constexpr (!Cfg::kOnesRow) ls[n] += pv;
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((((i & 63) >> 3) ^ (n & 7)) << 4)) =
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((ci ^ (n & 7)) << 4)) =
             __float2bfloat16_rn(pv);
       }
       fence_proxy_async_smem();
@@ -883,27 +885,31 @@ static cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap,
   return cudaLaunchKernelEx(&cfg, verify_tc_kernel<D, NQP, NQC, CAP>, kmap, vmap, p);
 }
 
-// Column tiles of 8: the processed columns NQC and the MMA width NQP.
+// The softmax's columns NQC = nq rounded up to 8, and the MMA width NQP (with
+// capture the two summed-query columns NQC, NQC + 1 come on top).
 template <int D, bool CAP>
 static cudaError_t launch_tc_cols(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                  const VerifyParams& p, int ncols, int batch, cudaStream_t s,
-                                  bool launch, int* clusters) {
-  switch ((ncols + 7) / 8) {
-    case 1: return launch_tc<D, 16, 8, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    case 2: return launch_tc<D, 16, 16, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    case 3: return launch_tc<D, 32, 24, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    case 4: return launch_tc<D, 32, 32, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    case 5: return launch_tc<D, 64, 40, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-    default: break;
-  }
+                                  const VerifyParams& p, int batch, cudaStream_t s, bool launch,
+                                  int* clusters) {
+  if (!verify_tc_supported(D, p.nq, CAP)) return cudaErrorInvalidValue;
+  const int nqc = (p.nq + 7) / 8 * 8, nqp = verify_tc_mma_columns(p.nq, CAP);
+#define VEGAS_TC_CASE(P_, C_)                                                    \
+  if constexpr (C_ + (CAP ? 2 : 0) <= P_)                                        \
+    if (nqp == P_ && nqc == C_)                                                  \
+      return launch_tc<D, P_, C_, CAP>(kmap, vmap, p, batch, s, launch, clusters);
+  VEGAS_TC_CASE(16, 8)
+  VEGAS_TC_CASE(16, 16)
+  VEGAS_TC_CASE(32, 16)
+  VEGAS_TC_CASE(32, 24)
+  VEGAS_TC_CASE(32, 32)
+  VEGAS_TC_CASE(64, 32)
+  VEGAS_TC_CASE(64, 40)
   if constexpr (D == 64) {
-    switch ((ncols + 7) / 8) {
-      case 6: return launch_tc<D, 64, 48, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-      case 7: return launch_tc<D, 64, 56, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-      case 8: return launch_tc<D, 64, 64, CAP>(kmap, vmap, p, batch, s, launch, clusters);
-      default: break;
-    }
+    VEGAS_TC_CASE(64, 48)
+    VEGAS_TC_CASE(64, 56)
+    VEGAS_TC_CASE(64, 64)
   }
+#undef VEGAS_TC_CASE
   return cudaErrorInvalidValue;
 }
 
@@ -912,23 +918,21 @@ static cudaError_t launch_tc_cols(const CUtensorMap& kmap, const CUtensorMap& vm
 
 cudaError_t VEGAS_CAT(launch_verify_tc_d, VEGAS_TC_D)(const CUtensorMap& kmap,
                                                      const CUtensorMap& vmap,
-                                                     const VerifyParams& p, int ncols,
-                                                     bool capture, int batch,
-                                                     cudaStream_t stream) {
+                                                     const VerifyParams& p, bool capture,
+                                                     int batch, cudaStream_t stream) {
   constexpr int D = VEGAS_TC_D;
-  return capture ? launch_tc_cols<D, true>(kmap, vmap, p, ncols, batch, stream, true, nullptr)
-                 : launch_tc_cols<D, false>(kmap, vmap, p, ncols, batch, stream, true, nullptr);
+  return capture ? launch_tc_cols<D, true>(kmap, vmap, p, batch, stream, true, nullptr)
+                 : launch_tc_cols<D, false>(kmap, vmap, p, batch, stream, true, nullptr);
 }
 
-int VEGAS_CAT(verify_tc_max_active_clusters_d, VEGAS_TC_D)(int ncols, bool capture,
-                                                          int cluster) {
+int VEGAS_CAT(verify_tc_max_active_clusters_d, VEGAS_TC_D)(int nq, bool capture, int cluster) {
   constexpr int D = VEGAS_TC_D;
   if (cluster < 1 || cluster > kMaxVerifyCluster) return 0;
+  if (!verify_tc_supported(D, nq, capture)) return 0;
   constexpr int kDevices = 32;
-  // [device][capture][column tiles][cluster]: 0 unknown, -1 none, else the count
+  // [device][capture][column tiles of the softmax][cluster]: 0 unknown, -1 none, else the count
   static std::atomic<int> cache[kDevices][2][9][kMaxVerifyCluster + 1];
-  const int ct = (ncols + 7) / 8;
-  if (ct < 1 || ct > verify_tc_max_columns(D) / 8) return 0;
+  const int ct = (nq + 7) / 8;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return 0;
   std::atomic<int>& slot = cache[dev][capture ? 1 : 0][ct][cluster];
@@ -936,13 +940,14 @@ int VEGAS_CAT(verify_tc_max_active_clusters_d, VEGAS_TC_D)(int ncols, bool captu
   if (c == 0) {
     VerifyParams p{};
     p.hkv = 1;
+    p.nq = nq;
     p.num_splits = cluster;
     p.cluster_size = cluster;
     p.cluster_merge = 1;
     CUtensorMap none{};
     int n = 0;
-    cudaError_t e = capture ? launch_tc_cols<D, true>(none, none, p, ncols, 1, 0, false, &n)
-                            : launch_tc_cols<D, false>(none, none, p, ncols, 1, 0, false, &n);
+    cudaError_t e = capture ? launch_tc_cols<D, true>(none, none, p, 1, 0, false, &n)
+                            : launch_tc_cols<D, false>(none, none, p, 1, 0, false, &n);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       n = 0;

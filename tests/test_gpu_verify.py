@@ -138,10 +138,11 @@ def test_cluster_merged_shape_needs_no_workspace():
 
 
 def test_several_clusters_per_unit_merge_through_the_workspace():
-    """Few units (8 at batch 1): each unit's splits form several clusters, merged
-    on chip within a cluster and through a few workspace rows across clusters;
-    repeated calls leave the tickets at zero and give identical results."""
-    c = Case(C2.with_(ctx_lo=5000, ctx_hi=5000))
+    """Few units (2 KV heads at batch 1): each unit's splits form several
+    clusters, merged on chip within a cluster and through a few workspace rows
+    across clusters; repeated calls leave the tickets at zero and give identical
+    results."""
+    c = Case(C2.with_(ctx_lo=5000, ctx_hi=5000, hkv=2, hq=8))
     w = c.w
     nb = vg.vegas_verify_workspace_size(c.kv, w.batch, w.gamma)
     assert nb > 0
