@@ -712,6 +712,16 @@ def run_gpu(args, rank, world, dist, peak, peak_kind):
     stages = stage_times(torch, it, stream, chunk)
     stages["source"] = ("external CUDA events at the stage boundaries of a separately "
                         "replayed graph (events there serialise the stages)")
+    if args.profile:
+        # the timed region and the stages only: every other leg is left out so
+        # that a profiler run holds just this workload's memory and launches
+        vb = per_call_us(torch, stream, lambda i: it.verify(i % it.R), 4 * it.R)
+        vp = per_call_us(torch, stream, lambda i: it.verify(i % it.R, capture=False), 4 * it.R)
+        sl = per_call_us(torch, stream, lambda i: it.select(), 8)
+        variants = {"verify_capture2_us": round(vb, 3), "verify_no_capture_us": round(vp, 3),
+                    "select_us": round(sl, 3)}
+        e2e = None
+        return (it, nbytes, ms_step, K_eff, stages, timing, clocks, e2e, variants, {})
     e2e = run_e2e(it, stream, min(K_eff, 500), nbytes)
     variants = time_variants(it, stream)
     variants["layer_stack_8"] = time_stack(w, 8, dev, stream, variants["verify_no_capture_us"])
@@ -938,6 +948,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="only the headline workload (no extra workloads)")
+    ap.add_argument("--profile", action="store_true",
+                    help="timed region, stages and back-to-back verify/select only (profiler runs)")
     ap.add_argument("--workload", default=WORKLOAD.name, choices=sorted(configs.BY_NAME),
                     help="the headline workload (default: the Qwen3-8B layer, batch 1, 32K)")
     args = ap.parse_args()
@@ -1012,7 +1024,7 @@ def main():
     line["variants"] = variants
     if extra:
         line["workloads"] = extra
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         ref = time_oracle(w, nbytes, budget_s=15.0, warmup=1)
         line["cpu_baseline"] = {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample",
                                                     "cpu_model")}

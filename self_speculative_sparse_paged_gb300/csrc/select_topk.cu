@@ -352,46 +352,30 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     uint32_t* mx = bmx + s * kBins;
     uint32_t* su = sup + s * kMaxSelCluster * kSuper;
     const int lo = mode == kKeyBits ? max(0, (32 - __clz(khi - klo)) - 11) : 0;
-    // Lanes of a warp that hit the same bin add to it once (match + popc, and
-    // for the bounds a warp min / max): scores bunch into few bins, and
-    // per-lane shared-memory atomics on one address serialise.
 #pragma unroll
     for (int u = 0; u < P; ++u) {
       const int r = r0 + u * 32;
-      const bool valid = r < nvalid;
-      const uint32_t key = valid ? keys[r] : 0u;
-      bool take = valid;
+      if (r >= nvalid) continue;
+      const uint32_t key = keys[r];
       uint32_t d;
       if (mode == kKeyBits) {
-        take = take && key >= klo && key <= khi;
+        if (key < klo || key > khi) continue;
         d = (key - klo) >> lo;
       } else {
         const float t = __fmul_rn(__fsub_rn(key_value(key), vmin), scale);
         const uint32_t bin = min((uint32_t)kBins - 1u, __float2uint_rz(fmaxf(0.f, t)));
         if (mode == kValueBins) {       // counts only: every key takes part
-          d = bin;
-        } else {
-          take = take && bin == vbin;
-          // t - vbin is exact (Sterbenz) and the scaling by 2048 too: monotone in the key
-          d = min((uint32_t)kBins - 1u,
-                  __float2uint_rz(fmaxf(0.f, __fmul_rn(__fsub_rn(t, float(vbin)), float(kBins)))));
+          atomicAdd(&c[bin], 1u);
+          continue;
         }
+        if (bin != vbin) continue;
+        // t - vbin is exact (Sterbenz) and the scaling by 2048 too: monotone in the key
+        d = min((uint32_t)kBins - 1u,
+                __float2uint_rz(fmaxf(0.f, __fmul_rn(__fsub_rn(t, float(vbin)), float(kBins)))));
       }
-      const uint32_t act = __ballot_sync(0xffffffffu, take);
-      if (take) {
-        const uint32_t peers = __match_any_sync(act, d);
-        const bool leader = __ffs(peers) - 1 == lane;
-        if (mode == kValueBins) {
-          if (leader) atomicAdd(&c[d], (uint32_t)__popc(peers));
-        } else {
-          const uint32_t a = __reduce_min_sync(peers, key), z = __reduce_max_sync(peers, key);
-          if (leader) {
-            atomicAdd(&c[d], (uint32_t)__popc(peers));
-            atomicMin(&mn[d], a);
-            atomicMax(&mx[d], z);
-          }
-        }
-      }
+      atomicAdd(&c[d], 1u);
+      atomicMin(&mn[d], key);
+      atomicMax(&mx[d], key);
     }
     __syncthreads();
     // super-bin sums: warp w adds super-bins 4w .. 4w + 3 and pushes each
