@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     st.in[tid] = 0u;
   }
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
+#pragma unroll 1
   for (int u0 = 0; u0 < P; u0 += 8) {
     if (u0 > 0) {
 #pragma unroll
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     uint32_t* mx = bmx + s * kBins;
     uint32_t* su = sup + s * kMaxSelCluster * kSuper;
     const int lo = mode == kKeyBits ? max(0, (32 - __clz(khi - klo)) - 11) : 0;
-#pragma unroll
+#pragma unroll 8
     for (int u = 0; u < P; ++u) {
       const int r = r0 + u * 32;
       if (r >= nvalid) continue;
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
 
   // ---- compaction in position order: per-warp counts, then ballot ranks
   uint32_t n_gt = 0, n_eq = 0;
-#pragma unroll
+#pragma unroll 8
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
     const bool valid = r < nvalid;
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   gt += red[warp];
   eq += red[kSelWarps + warp];
   const uint32_t below = (1u << lane) - 1u;
-#pragma unroll
+#pragma unroll 8
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
     const bool valid = r < nvalid;

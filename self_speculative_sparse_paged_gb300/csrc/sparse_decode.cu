@@ -29,7 +29,9 @@ namespace vegas {
 
 template <int D>
 struct SparseCfg {
-  static constexpr int kStages = 2;
+  // 16-row groups in flight per warp: a head_dim-64 group is half the bytes of
+  // a head_dim-128 one, so it keeps twice as many in flight
+  static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr int kRow = D * 2 + 16;           // padded row stride
   static constexpr int kTile = 16 * kRow;
   static constexpr int kStage = 2 * kTile;

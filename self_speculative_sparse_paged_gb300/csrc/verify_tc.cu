@@ -362,7 +362,10 @@ __global__ void __launch_bounds__(384, 1)
     // The whole warp runs the loop, so its control flow and the operand
     // descriptors stay warp-uniform; one elected lane issues and commits.
     constexpr uint32_t idS = idesc_bf16(128, NQP, 0, 0);
-    constexpr uint32_t idPV = idesc_bf16(128, NQP, 1, 0);   // M = 128 dims (padded at D = 64)
+    // M = 128 dims (padded at D = 64); P^T is MN-major (one 128-byte row of
+    // 64 columns per position) when NQP = 64, else K-major
+    constexpr bool kPmn = NQP == 64;
+    constexpr uint32_t idPV = idesc_bf16(128, NQP, 1, kPmn ? 1 : 0);
     const bool leader = elect_one();
     // Descriptors without their start address; the address field (bits 0-13)
     // holds (address / 16) mod 2^14, the part of a shared-window address the
@@ -385,7 +388,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kp = 0; kp < 8; ++kp)
           tc_mma(tmem + 2 * kCol + kCol * gg, with_addr(dVmn, vb + kp * 128),
-                 with_addr(dSw, pb + (kp >> 2) * (NQP * 8) + (kp & 3) * 2), idPV, t >= 2 || kp > 0);
+                 kPmn ? with_addr(dVmn, pb + kp * 128)
+                      : with_addr(dSw, pb + (kp >> 2) * (NQP * 8) + (kp & 3) * 2),
+                 idPV, t >= 2 || kp > 0);
         tc_commit(pvdone(gg));
         tc_commit(vfree(s));
       }
@@ -590,20 +595,51 @@ __global__ void __launch_bounds__(384, 1)
       }
       // P^T operand, K-major with the 128-byte swizzle: element (n, i) at
       // (i / 64) * NQP * 128 + n * 128 + (((i % 64) / 8) ^ (n % 8)) * 16 + (i % 8) * 2.
-      // (row n, chunk c ^ (n % 8)): eight chunk offsets cover every n
-      uint8_t* pbuf = smem + Cfg::kOffP + grp * Cfg::kP + (i >> 6) * (NQP * 128) + (i & 7) * 2;
-      const int ci = (i & 63) >> 3;
+      if constexpr (NQP == 64) {
+        // P^T MN-major: position i's row of 64 columns, eight 16-byte chunks
+        // (eight bf16 columns each, one store per chunk), chunk c at c ^ (i % 8)
+        // (128-byte swizzle); columns past NQC are 0
+        uint8_t* prow = smem + Cfg::kOffP + grp * Cfg::kP + i * 128;
 #pragma unroll
-      for (int n = 0; n < NQC; ++n) {
-        float mn;
-        if constexpr (kSmemMax)
-          mn = mg[n];
-        else
-          mn = m[n];
-        const float pv = ex2(x[n] - mn);
-        if constexpr (!Cfg::kOnesRow) ls[n] += pv;
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((ci ^ (n & 7)) << 4)) =
-            __float2bfloat16_rn(pv);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w4[4] = {0u, 0u, 0u, 0u};
+          if (8 * c < NQC) {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              float pe[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int n = 8 * c + e + h;
+                float mn;
+                if constexpr (kSmemMax)
+                  mn = mg[n];
+                else
+                  mn = m[n];
+                pe[h] = ex2(x[n] - mn);
+                if constexpr (!Cfg::kOnesRow) ls[n] += pe[h];
+              }
+              w4[e / 2] = pack_bf16x2(pe[0], pe[1]);
+            }
+          }
+          *reinterpret_cast<uint4*>(prow + ((c ^ (i & 7)) << 4)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      } else {
+        // P^T K-major: (row n, chunk c ^ (n % 8)); eight chunk offsets cover every n
+        uint8_t* pbuf = smem + Cfg::kOffP + grp * Cfg::kP + (i >> 6) * (NQP * 128) + (i & 7) * 2;
+        const int ci = (i & 63) >> 3;
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) {
+          float mn;
+          if constexpr (kSmemMax)
+            mn = mg[n];
+          else
+            mn = m[n];
+          const float pv = ex2(x[n] - mn);
+          if constexpr (!Cfg::kOnesRow) ls[n] += pv;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((ci ^ (n & 7)) << 4)) =
+              __float2bfloat16_rn(pv);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
