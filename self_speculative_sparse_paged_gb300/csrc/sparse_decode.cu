@@ -43,7 +43,7 @@ template <int D, int NT>
 constexpr size_t sparse_smem_layout_bytes() {
   return SparseCfg<D>::kStageBytes                                 // stages
          + size_t(NT) * 8 * (2 * D + 16)                           // Q tile
-         + size_t(kAttnWarps) * SparseCfg<D>::kStages * 8          // mbarriers
+         + (size_t(kAttnWarps) * SparseCfg<D>::kStages + 1) * 8    // mbarriers (+ receive)
          + size_t(SparseCfg<D>::kMaxRows) * 4                      // row table
          + size_t(NT) * 8 * (D + 2) * 4                            // CTA partial
          + (size_t(NT) * 8 * D + kMaxSparseCluster) * 4              // received output slices
@@ -63,10 +63,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   constexpr int QROW = 2 * D + 16;
   using Tile = PaddedTile<D>;
 
-  // First phase of the cluster barrier: this CTA has started (its shared
-  // memory may receive other CTAs' stores once every CTA has arrived).
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  griddep_begin();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
@@ -77,7 +73,23 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   uint8_t* stage_area = smem;
   uint8_t* qs = smem + SparseCfg<D>::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(qs + NPAD * QROW);
-  int32_t* rows = reinterpret_cast<int32_t*>(bars + W * STAGES);
+  uint64_t* recv_bar = bars + W * STAGES;   // completes when every peer's state has landed
+  int32_t* rows = reinterpret_cast<int32_t*>(recv_bar + 1);
+  const int nel = p.group * D;              // output elements of the unit (G x D)
+  const int per = (nel + CL - 1) / CL;      // CTA r owns [r * per, (r + 1) * per)
+  if (threadIdx.x == 0) {
+    // Every CTA sends this one its slice of the partial output and its G row
+    // maxima and sums: 4 * CL * (slice + 2G) bytes, counted by st.async.
+    mbar_init(smem_u32(recv_bar), 1);
+    const int mine = max(0, min(per, nel - rank * per));
+    mbar_arrive_expect_tx(smem_u32(recv_bar), uint32_t(4 * CL * (mine + 2 * p.group)));
+    fence_mbar_init();
+  }
+  // First phase of the cluster barrier: this CTA has started and its receive
+  // barrier is set up (its shared memory may receive other CTAs' stores once
+  // every CTA has arrived).
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  griddep_begin();
   float* pM = reinterpret_cast<float*>(rows + SparseCfg<D>::kMaxRows);   // [NPAD] CTA partial
   float* pL = pM + NPAD;                                                 // [NPAD]
   float* pO = pL + NPAD;                                                 // [NPAD][D]
@@ -239,30 +251,34 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
 
   // Cluster merge: CTA r owns the output elements [r * per, (r + 1) * per) of
   // the G x D.  Every CTA pushes the slices of its state to their owners'
-  // receive areas with distributed-shared-memory stores (each thread the
-  // elements it merged above, threads n < G the row maxima and sums), one
-  // cluster barrier publishes them, and each owner merges locally:
+  // receive areas with asynchronous distributed-shared-memory stores (each
+  // thread the elements it merged above, threads n < G the row maxima and
+  // sums), each counted against the owner's receive barrier; an owner merges
+  // as soon as its barrier has counted every byte it expects:
   // M = max_r m_r, O = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r.
   // The receive areas are used by nothing else, so only the barrier phase
-  // begun at entry (every CTA has started) precedes the stores.
-  const int nel = p.group * D;
-  const int per = (nel + CL - 1) / CL;
+  // begun at entry (every CTA has started, its receive barrier is ready)
+  // precedes the stores, and no cluster barrier follows them.
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   {
     const uint32_t rO_s = smem_u32(rO), rM_s = smem_u32(rM), rL_s = smem_u32(rL);
+    const uint32_t rb = smem_u32(recv_bar);
     for (int e = tid; e < nel; e += NTH) {
       const int owner = e / per;
-      st_cluster_f32(cluster_map(rO_s + 4 * (rank * per + e - owner * per), owner), pO[e]);
+      st_async_f32(cluster_map(rO_s + 4 * (rank * per + e - owner * per), owner), pO[e],
+                   cluster_map(rb, owner));
     }
     if (tid < p.group) {
       for (int r = 0; r < CL; ++r) {
-        st_cluster_f32(cluster_map(rM_s + 4 * (rank * NPAD + tid), r), pM[tid]);
-        st_cluster_f32(cluster_map(rL_s + 4 * (rank * NPAD + tid), r), pL[tid]);
+        st_async_f32(cluster_map(rM_s + 4 * (rank * NPAD + tid), r), pM[tid], cluster_map(rb, r));
+        st_async_f32(cluster_map(rL_s + 4 * (rank * NPAD + tid), r), pL[tid], cluster_map(rb, r));
       }
     }
   }
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (!mbar_wait_cluster_bounded(smem_u32(recv_bar), 0)) {
+    if (tid == 0) set_error(p.err, kErrDeviceTimeout);
+    return;
+  }
   {
     constexpr int R = kMaxSparseCluster;
     const int e0 = rank * per, e1 = min(nel, e0 + per);

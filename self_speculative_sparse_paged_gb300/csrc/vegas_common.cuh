@@ -302,6 +302,35 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+// Asynchronous store into another CTA's shared memory that, once written,
+// counts its 4 bytes against the transaction count of the mbarrier at
+// `remote_bar` (both addresses from cluster_map).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr),
+               "f"(v), "r"(remote_bar)
+               : "memory");
+}
+// mbar_wait_for at cluster scope: the phase's completion was caused by other
+// CTAs of the cluster (remote transaction counts), whose writes it makes visible.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity) {
+  auto ready = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (ready()) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    if (ready()) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
 
 // True in exactly one lane of the (fully active) warp.
 __device__ __forceinline__ bool elect_one() {

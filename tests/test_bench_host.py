@@ -7,16 +7,16 @@ from workload import configs, gen
 
 
 def test_roofline_entry_fields_and_arithmetic():
-    r = bench.roofline_entry(135_368_704, 34.88, 6795.5, "measured", back_to_back_us=29.56)
+    r = bench.roofline_entry(135_368_704, 29.56, 6795.5, "measured", stage_us=34.88)
     for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert k in r
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
-    assert math.isclose(r["achieved"], 135_368_704 / 34.88e-6 / 1e9, rel_tol=1e-4)
+    assert math.isclose(r["achieved"], 135_368_704 / 29.56e-6 / 1e9, rel_tol=1e-4)
     assert math.isclose(r["frac"], r["achieved"] / 6795.5, rel_tol=1e-3)
-    b = r["back_to_back"]
-    assert b["achieved"] > r["achieved"] and math.isclose(b["frac"], b["achieved"] / 6795.5,
-                                                          rel_tol=1e-3)
-    assert "back_to_back" not in bench.roofline_entry(1e8, 10.0, 6795.5, "measured")
+    st = r["stage_events"]
+    assert st["achieved"] < r["achieved"] and math.isclose(st["frac"], st["achieved"] / 6795.5,
+                                                           rel_tol=1e-3)
+    assert "stage_events" not in bench.roofline_entry(1e8, 10.0, 6795.5, "measured")
 
 
 def test_traffic_is_null_or_the_recorded_capture():
