@@ -442,6 +442,12 @@ __global__ void __launch_bounds__(384, 1)
       if (i < NQC) mg[i] = kEmptyMax;
       named_bar(1 + grp, 128);
     }
+    auto mcol = [&](int n) {
+      if constexpr (kSmemMax)
+        return mg[n];
+      else
+        return m[n];
+    };
     // Columns nq .. NQC - 1 multiply zero query rows: their logits are 0, they
     // never raise a maximum after the first tile and nothing reads their output.
     float* srow = CAPTURE ? p.scores + size_t(unit) * p.score_stride : nullptr;
@@ -457,6 +463,9 @@ __global__ void __launch_bounds__(384, 1)
       const int k = t >> 1, s = t % VS;
       bool okt = ok && mbar_wait_bounded(sfull(grp), k & 1);
       tc_fence_after();
+      const int page = pbeg + 8 * t + (i >> 4);
+      const bool live = page < pend;
+      const int pos = page * 16 + (i & 15);
       float x[NQC];
       float cx[2] = {0.f, 0.f};   // the two capture columns
 #pragma unroll
@@ -474,9 +483,6 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(sread(grp));
       }
-      const int page = pbeg + 8 * t + (i >> 4);
-      const bool live = page < pend;
-      const int pos = page * 16 + (i & 15);
       if (CAPTURE && okt && live && pos < Lcap) srow[pos] = (cx[0] + cx[1]) * p.scale;
       if (!CAPTURE && p.raw && okt && live && pos < min(L, p.raw_stride)) {
         // the pages' way: every captured row's logit of every head goes to memory
@@ -484,20 +490,6 @@ __global__ void __launch_bounds__(384, 1)
         for (int n = 0; n < NQC; ++n) {
           const int rr = rawrow[n];
           if (rr >= 0) p.raw[size_t(rr) * p.raw_stride + pos] = x[n] * p.scale;
-        }
-      }
-      const int lpos = (live ? page : pbeg + 8 * t) * 16 + (i & 15);   // position loaded in row i
-      if (okt && lpos > last_valid) {
-        // a cache slot past the window: zero its V row so 0 * garbage cannot be NaN
-        okt = mbar_wait_bounded(vfull(s), (t / VS) & 1);
-        uint8_t* vrow = smem + Cfg::kOffV + s * Cfg::kVS + i * 128;
-        if (okt) {
-#pragma unroll
-          for (int h = 0; h < Cfg::kHalves; ++h)
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-              *reinterpret_cast<uint4*>(vrow + h * 16384 + ((cc ^ (i & 7)) << 4)) =
-                  make_uint4(0, 0, 0, 0);
         }
       }
       // logits in log2 units; positions past the range, and window positions a
@@ -513,11 +505,20 @@ __global__ void __launch_bounds__(384, 1)
       }
       bool need = false;
 #pragma unroll
-      for (int n = 0; n < NQC; ++n) {
-        if constexpr (kSmemMax)
-          need |= x[n] > mg[n] + kRescaleSlack;
-        else
-          need |= x[n] > m[n] + kRescaleSlack;
+      for (int n = 0; n < NQC; ++n) need |= x[n] > mcol(n) + kRescaleSlack;
+      const int lpos = (live ? page : pbeg + 8 * t) * 16 + (i & 15);   // position loaded in row i
+      if (okt && lpos > last_valid) {
+        // a cache slot past the window: zero its V row so 0 * garbage cannot be NaN
+        okt = mbar_wait_bounded(vfull(s), (t / VS) & 1);
+        uint8_t* vrow = smem + Cfg::kOffV + s * Cfg::kVS + i * 128;
+        if (okt) {
+#pragma unroll
+          for (int h = 0; h < Cfg::kHalves; ++h)
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              *reinterpret_cast<uint4*>(vrow + h * 16384 + ((cc ^ (i & 7)) << 4)) =
+                  make_uint4(0, 0, 0, 0);
+        }
       }
       const int wvote = (__any_sync(0xffffffffu, need) ? 1 : 0) | (__any_sync(0xffffffffu, !okt) ? 2 : 0);
       if (lane == 0) votes[grp * 4 + q4] = wvote;
@@ -544,57 +545,34 @@ __global__ void __launch_bounds__(384, 1)
         auto new_max = [&](int n, float mold) {
           return fmaxf(mold, fmaxf(fmaxf(cm[n], cm[NQC + n]), fmaxf(cm[2 * NQC + n], cm[3 * NQC + n])));
         };
-        if constexpr (!kSmemMax) {
-          float f[NQC];
+        // factors per 8-column chunk; O^T rescaled chunk by chunk
 #pragma unroll
-          for (int n = 0; n < NQC; ++n) {
-            const float mn = new_max(n, m[n]);
-            f[n] = ex2(m[n] - mn);
-            m[n] = mn;
-            if constexpr (!Cfg::kOnesRow) ls[n] *= f[n];
+        for (int c = 0; c < NQC / 8; ++c) {
+          float f8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int n = 8 * c + e;
+            const float mold = mcol(n), mn = new_max(n, mold);
+            f8[e] = ex2(mold - mn);
+            if constexpr (!kSmemMax) m[n] = mn;
+            if constexpr (!Cfg::kOnesRow) ls[n] *= f8[e];
           }
           if (k > 0 && pv_ok) {
-            // O^T row i of this group, columns scaled by f
+            float v8[8];
+            tmem_ld8(tl + o_col + 8 * c, v8);
+            tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < NQC / 8; ++c) {
-              float v8[8];
-              tmem_ld8(tl + o_col + 8 * c, v8);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] *= f[8 * c + e];
-              tmem_st8(tl + o_col + 8 * c, v8);
-            }
-            tmem_st_wait();
+            for (int e = 0; e < 8; ++e) v8[e] *= f8[e];
+            tmem_st8(tl + o_col + 8 * c, v8);
           }
-          named_bar(1 + grp, 128);   // colmax is rewritten at the next rescale
-        } else {
-          // factors recomputed per 8-column chunk from the old maxima in mrun
-#pragma unroll
-          for (int c = 0; c < NQC / 8; ++c) {
-            float f8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float mold = mg[8 * c + e];
-              f8[e] = ex2(mold - new_max(8 * c + e, mold));
-              if constexpr (!Cfg::kOnesRow) ls[8 * c + e] *= f8[e];
-            }
-            if (k > 0 && pv_ok) {
-              float v8[8];
-              tmem_ld8(tl + o_col + 8 * c, v8);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] *= f8[e];
-              tmem_st8(tl + o_col + 8 * c, v8);
-            }
-          }
-          if (k > 0 && pv_ok) tmem_st_wait();
-          named_bar(1 + grp, 128);   // every thread has read the old maxima
+        }
+        if (k > 0 && pv_ok) tmem_st_wait();
+        named_bar(1 + grp, 128);   // colmax (and mrun) read; colmax is rewritten at the next rescale
+        if constexpr (kSmemMax) {
           if (i < NQC) mg[i] = new_max(i, mg[i]);
-          named_bar(1 + grp, 128);   // new maxima visible; colmax free again
+          named_bar(1 + grp, 128);   // new maxima visible
         }
       }
-      // P^T operand, K-major with the 128-byte swizzle: element (n, i) at
-      // (i / 64) * NQP * 128 + n * 128 + (((i % 64) / 8) ^ (n % 8)) * 16 + (i % 8) * 2.
       if constexpr (NQP == 64) {
         // P^T MN-major: position i's row of 64 columns, eight 16-byte chunks
         // (eight bf16 columns each, one store per chunk), chunk c at c ^ (i % 8)
@@ -606,36 +584,26 @@ __global__ void __launch_bounds__(384, 1)
           if (8 * c < NQC) {
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-              float pe[2];
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int n = 8 * c + e + h;
-                float mn;
-                if constexpr (kSmemMax)
-                  mn = mg[n];
-                else
-                  mn = m[n];
-                pe[h] = ex2(x[n] - mn);
-                if constexpr (!Cfg::kOnesRow) ls[n] += pe[h];
+              const int n = 8 * c + e;
+              const float p0 = ex2(x[n] - mcol(n)), p1 = ex2(x[n + 1] - mcol(n + 1));
+              if constexpr (!Cfg::kOnesRow) {
+                ls[n] += p0;
+                ls[n + 1] += p1;
               }
-              w4[e / 2] = pack_bf16x2(pe[0], pe[1]);
+              w4[e / 2] = pack_bf16x2(p0, p1);
             }
           }
           *reinterpret_cast<uint4*>(prow + ((c ^ (i & 7)) << 4)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       } else {
-        // P^T K-major: (row n, chunk c ^ (n % 8)); eight chunk offsets cover every n
+        // P^T K-major: element (n, i) at (i / 64) * NQP * 128 + n * 128 +
+        // (((i % 64) / 8) ^ (n % 8)) * 16 + (i % 8) * 2 (128-byte swizzle)
         uint8_t* pbuf = smem + Cfg::kOffP + grp * Cfg::kP + (i >> 6) * (NQP * 128) + (i & 7) * 2;
         const int ci = (i & 63) >> 3;
 #pragma unroll
         for (int n = 0; n < NQC; ++n) {
-          float mn;
-          if constexpr (kSmemMax)
-            mn = mg[n];
-          else
-            mn = m[n];
-          const float pv = ex2(x[n] - mn);
+          const float pv = ex2(x[n] - mcol(n));
           if constexpr (!Cfg::kOnesRow) ls[n] += pv;
           *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((ci ^ (n & 7)) << 4)) =
               __float2bfloat16_rn(pv);
