@@ -75,9 +75,9 @@ struct TcCfg {
   static constexpr int kNumBars = 2 * KS + 2 * VS + 4 * 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // misc: tmem slot, flag, votes[2][4], colmax[2][4][NQC], colsum[2][4][NQC], tlim[NQP],
-  // rawrow[NQP], running maxima mrun[2][NQC] (kept there instead of registers when NQC > 32)
-  static constexpr size_t kMisc = 16 + 32 + 4 * (18 * NQC + 2 * NQP);
+  // rawrow[NQP], negated column references nref[2][NQC] (wide tiles, on the next 16-byte boundary)
   static constexpr bool kSmemMax = NQC > 32;
+  static constexpr size_t kMisc = 16 + 32 + 4 * (18 * NQC + 2 * NQP) + (kSmemMax ? 16 : 0);
   static constexpr size_t kSmem = size_t(kOffMisc) + kMisc + 1024;
 };
 
@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(384, 1)
   float* colsum = colmax + 8 * NQC;                              // [2][4][NQC]
   int* tlim = reinterpret_cast<int*>(colsum + 8 * NQC);          // [NQP]
   int* rawrow = tlim + NQP;                                      // [NQP] raw-logit row of a column, or -1
-  float* mrun = reinterpret_cast<float*>(rawrow + NQP);          // [2][NQC] running maxima (wide tiles)
+  float* mrun = reinterpret_cast<float*>(                        // [2][NQC] nref (wide tiles)
+      (reinterpret_cast<uintptr_t>(rawrow + NQP) + 15) & ~uintptr_t(15));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -427,29 +428,31 @@ __global__ void __launch_bounds__(384, 1)
     const int i = 32 * q4 + lane;             // tile position / head dimension owned
     const uint32_t tl = tmem + (uint32_t(32 * q4) << 16);
     const uint32_t s_col = kCol * grp, o_col = 2 * kCol + kCol * grp;
-    // Running maxima per column: registers, or (wide tiles) the group's mrun row,
-    // read by broadcast; row sums per column and thread, unless V's ones row
-    // makes the PV MMA accumulate them.
-    constexpr bool kSmemMax = Cfg::kSmemMax;
-    float m[kSmemMax ? 1 : NQC], ls[Cfg::kOnesRow ? 1 : NQC];
+    // Narrow tiles (at most 32 columns) keep each column's running maximum m
+    // in registers and take P = 2^(x * scale_log2 - m).  Wide tiles, where the
+    // softmax's instruction count sets the pace, keep per column a reference r
+    // (m, or 0 while the column has seen no unmasked logit: m = kEmptyMax) as
+    // -r in the group's nref row of shared memory, read as 16-byte vectors,
+    // and take y = x * scale_log2 - r in one FMA, so that P = 2^y needs no
+    // other per-element step and the rescale test is the largest y against
+    // the slack; `empty` flags the columns still without a maximum (identical
+    // in every thread of the group).  Row sums per column and thread are kept
+    // unless V's ones row makes the PV MMA accumulate them.
+    constexpr bool kOffset = Cfg::kSmemMax;
+    float m[kOffset ? 1 : NQC], ls[Cfg::kOnesRow ? 1 : NQC];
 #pragma unroll
     for (int n = 0; n < NQC; ++n) {
-      if constexpr (!kSmemMax) m[n] = kEmptyMax;
+      if constexpr (!kOffset) m[n] = kEmptyMax;
       if constexpr (!Cfg::kOnesRow) ls[n] = 0.f;
     }
-    float* mg = mrun + grp * NQC;
-    if constexpr (kSmemMax) {
-      if (i < NQC) mg[i] = kEmptyMax;
+    float* nrg = mrun + grp * NQC;
+    if constexpr (kOffset) {
+      if (i < NQC) nrg[i] = 0.f;
       named_bar(1 + grp, 128);
     }
-    auto mcol = [&](int n) {
-      if constexpr (kSmemMax)
-        return mg[n];
-      else
-        return m[n];
-    };
-    // Columns nq .. NQC - 1 multiply zero query rows: their logits are 0, they
-    // never raise a maximum after the first tile and nothing reads their output.
+    uint64_t empty = NQC == 64 ? ~0ull : (1ull << NQC) - 1;
+    // Columns nq .. NQC - 1 multiply zero query rows: their logits are 0 and
+    // nothing reads their output.
     float* srow = CAPTURE ? p.scores + size_t(unit) * p.score_stride : nullptr;
     int Lcap = L;
     if (CAPTURE && L > p.score_stride) {
@@ -466,17 +469,17 @@ __global__ void __launch_bounds__(384, 1)
       const int page = pbeg + 8 * t + (i >> 4);
       const bool live = page < pend;
       const int pos = page * 16 + (i & 15);
-      float x[NQC];
+      float y[NQC];
       float cx[2] = {0.f, 0.f};   // the two capture columns
 #pragma unroll
-      for (int n = 0; n < NQC; ++n) x[n] = 0.f;
+      for (int n = 0; n < NQC; ++n) y[n] = 0.f;
       if (okt) {
 #pragma unroll
         for (int c = 0; c < NQC / 8; ++c) {
           float v8[8];
           tmem_ld8(tl + s_col + 8 * c, v8);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[8 * c + e] = v8[e];
+          for (int e = 0; e < 8; ++e) y[8 * c + e] = v8[e];
         }
         if constexpr (CAPTURE) tmem_ld2(tl + s_col + cap0, cx);
         tmem_ld_wait();
@@ -489,23 +492,45 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int n = 0; n < NQC; ++n) {
           const int rr = rawrow[n];
-          if (rr >= 0) p.raw[size_t(rr) * p.raw_stride + pos] = x[n] * p.scale;
+          if (rr >= 0) p.raw[size_t(rr) * p.raw_stride + pos] = y[n] * p.scale;
         }
       }
-      // logits in log2 units; positions past the range, and window positions a
-      // row may not see yet (pos > L + t), are masked
-      const float sl2 = live ? p.scale_log2 : 0.f;
-      const float bias = live ? 0.f : -INFINITY;
-#pragma unroll
-      for (int n = 0; n < NQC; ++n) x[n] = fmaf(x[n], sl2, bias);
-      if (pos > L) {
-#pragma unroll
-        for (int n = 0; n < NQC; ++n)
-          if (pos > L + tlim[n]) x[n] = -INFINITY;
-      }
+      // logits in log2 units (less the reference, wide tiles); positions past
+      // the split's range, and window positions a row may not see yet
+      // (pos > L + t), are masked
       bool need = false;
+      if constexpr (kOffset) {
+        const float4* nr4 = reinterpret_cast<const float4*>(nrg);
 #pragma unroll
-      for (int n = 0; n < NQC; ++n) need |= x[n] > mcol(n) + kRescaleSlack;
+        for (int c = 0; c < NQC / 4; ++c) {
+          const float4 v = nr4[c];
+          y[4 * c + 0] = fmaf(y[4 * c + 0], p.scale_log2, v.x);
+          y[4 * c + 1] = fmaf(y[4 * c + 1], p.scale_log2, v.y);
+          y[4 * c + 2] = fmaf(y[4 * c + 2], p.scale_log2, v.z);
+          y[4 * c + 3] = fmaf(y[4 * c + 3], p.scale_log2, v.w);
+        }
+        if (!live || pos > L) {
+#pragma unroll
+          for (int n = 0; n < NQC; ++n)
+            if (!live || pos > L + tlim[n]) y[n] = -INFINITY;
+        }
+        float ym[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) ym[n & 3] = fmaxf(ym[n & 3], y[n]);
+        need = fmaxf(fmaxf(ym[0], ym[1]), fmaxf(ym[2], ym[3])) > kRescaleSlack;
+      } else {
+        const float sl2 = live ? p.scale_log2 : 0.f;
+        const float bias = live ? 0.f : -INFINITY;
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) y[n] = fmaf(y[n], sl2, bias);
+        if (pos > L) {
+#pragma unroll
+          for (int n = 0; n < NQC; ++n)
+            if (pos > L + tlim[n]) y[n] = -INFINITY;
+        }
+#pragma unroll
+        for (int n = 0; n < NQC; ++n) need |= y[n] > m[n] + kRescaleSlack;
+      }
       const int lpos = (live ? page : pbeg + 8 * t) * 16 + (i & 15);   // position loaded in row i
       if (okt && lpos > last_valid) {
         // a cache slot past the window: zero its V row so 0 * garbage cannot be NaN
@@ -532,29 +557,43 @@ __global__ void __launch_bounds__(384, 1)
       // is rescaled or its P^T buffer rewritten.
       bool pv_ok = k == 0 || mbar_wait_bounded(pvdone(grp), (k - 1) & 1);
       tc_fence_after();
-      if (allv & 1) {
+      if ((allv & 1) || (kOffset && empty)) {
+        // column maxima over the group's 128 positions
 #pragma unroll
         for (int n = 0; n < NQC; ++n) {
-          float v = x[n];
+          float v = y[n];
 #pragma unroll
           for (int o2 = 16; o2 > 0; o2 >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o2));
           if (lane == 0) colmax[(grp * 4 + q4) * NQC + n] = v;
         }
         named_bar(1 + grp, 128);
         const float* cm = colmax + grp * 4 * NQC;
-        auto new_max = [&](int n, float mold) {
-          return fmaxf(mold, fmaxf(fmaxf(cm[n], cm[NQC + n]), fmaxf(cm[2 * NQC + n], cm[3 * NQC + n])));
+        auto cmax = [&](int n) {
+          return fmaxf(fmaxf(cm[n], cm[NQC + n]), fmaxf(cm[2 * NQC + n], cm[3 * NQC + n]));
         };
-        // factors per 8-column chunk; O^T rescaled chunk by chunk
+        // Per 8-column chunk: the new maximum m', the factor 2^(m - m') for
+        // O^T and the row sums and (wide tiles) the new reference r', with y
+        // shifted to it.
+        uint64_t empty2 = empty;
 #pragma unroll
         for (int c = 0; c < NQC / 8; ++c) {
           float f8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int n = 8 * c + e;
-            const float mold = mcol(n), mn = new_max(n, mold);
-            f8[e] = ex2(mold - mn);
-            if constexpr (!kSmemMax) m[n] = mn;
+            if constexpr (kOffset) {
+              const float nro = nrg[n];
+              const float mold = ((empty >> n) & 1) ? kEmptyMax : -nro;
+              const float mnew = fmaxf(mold, cmax(n) - nro);
+              const bool now_empty = mnew == kEmptyMax;
+              f8[e] = ex2(mold - mnew);
+              if (!now_empty) empty2 &= ~(1ull << n);
+              y[n] += (now_empty ? 0.f : -mnew) - nro;
+            } else {
+              const float mnew = fmaxf(m[n], cmax(n));
+              f8[e] = ex2(m[n] - mnew);
+              m[n] = mnew;
+            }
             if constexpr (!Cfg::kOnesRow) ls[n] *= f8[e];
           }
           if (k > 0 && pv_ok) {
@@ -567,12 +606,25 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (k > 0 && pv_ok) tmem_st_wait();
-        named_bar(1 + grp, 128);   // colmax (and mrun) read; colmax is rewritten at the next rescale
-        if constexpr (kSmemMax) {
-          if (i < NQC) mg[i] = new_max(i, mg[i]);
-          named_bar(1 + grp, 128);   // new maxima visible
+        named_bar(1 + grp, 128);   // colmax (and nref) read; colmax is rewritten at the next rescale
+        if constexpr (kOffset) {
+          if (i < NQC) {
+            const float nro = nrg[i];
+            const float mold = ((empty >> i) & 1) ? kEmptyMax : -nro;
+            const float mnew = fmaxf(mold, cmax(i) - nro);
+            nrg[i] = mnew == kEmptyMax ? 0.f : -mnew;
+          }
+          named_bar(1 + grp, 128);   // new references visible
+          empty = empty2;
         }
       }
+      // P = 2^y (wide tiles) or 2^(y - m)
+      auto pcol = [&](int n) {
+        if constexpr (kOffset)
+          return ex2(y[n]);
+        else
+          return ex2(y[n] - m[n]);
+      };
       if constexpr (NQP == 64) {
         // P^T MN-major: position i's row of 64 columns, eight 16-byte chunks
         // (eight bf16 columns each, one store per chunk), chunk c at c ^ (i % 8)
@@ -585,7 +637,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
               const int n = 8 * c + e;
-              const float p0 = ex2(x[n] - mcol(n)), p1 = ex2(x[n + 1] - mcol(n + 1));
+              const float p0 = pcol(n), p1 = pcol(n + 1);
               if constexpr (!Cfg::kOnesRow) {
                 ls[n] += p0;
                 ls[n + 1] += p1;
@@ -603,7 +655,7 @@ __global__ void __launch_bounds__(384, 1)
         const int ci = (i & 63) >> 3;
 #pragma unroll
         for (int n = 0; n < NQC; ++n) {
-          const float pv = ex2(x[n] - mcol(n));
+          const float pv = pcol(n);
           if constexpr (!Cfg::kOnesRow) ls[n] += pv;
           *reinterpret_cast<__nv_bfloat16*>(pbuf + n * 128 + ((ci ^ (n & 7)) << 4)) =
               __float2bfloat16_rn(pv);
@@ -657,8 +709,8 @@ __global__ void __launch_bounds__(384, 1)
       const float* cs = colsum + grp * 4 * NQC;
       if (mytiles > 0)
         Lg = Cfg::kOnesRow ? cs[i] : cs[i] + cs[NQC + i] + cs[2 * NQC + i] + cs[3 * NQC + i];
-      if constexpr (kSmemMax) {
-        Mg = mg[i];
+      if constexpr (kOffset) {
+        Mg = ((empty >> i) & 1) ? kEmptyMax : -nrg[i];
       } else {
 #pragma unroll
         for (int n = 0; n < NQC; ++n)
