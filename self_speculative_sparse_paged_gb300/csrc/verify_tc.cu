@@ -53,23 +53,30 @@ struct TcCfg {
   // completes, a V slot only when its PV MMA does.  Under full HBM load a
   // tile's load latency reaches ~2 us, which each ring must cover on its own.
   // (Two K slots when 64 query columns at head_dim 128 leave no room for three.)
+  // (At head_dim 64 a V slot is half as large and the V ring is four deep: a
+  // V slot is held from its load until its PV MMA has completed, so one more
+  // slot keeps more of the stream in flight; five to seven slots, which let the
+  // V loads run further ahead of the K loads, measured slower.)
   static constexpr int KS = (D == 128 && NQP == 64) ? 2 : 3;
-  static constexpr int VS = 3;
+  static constexpr int VS = D == 64 ? 4 : 3;
   static constexpr int kHalves = D / 64;             // 64-column (128-byte) halves of a row
-  static constexpr int kKV = 128 * D * 2;            // one K tile (and the loaded part of V)
-  // A V slot always spans 128 head dimensions (two halves): at head_dim 64 the
-  // PV MMA keeps M = 128 with an upper half that is written once, all zeros
-  // except dimension 64, which holds ones so that O^T row 64 accumulates the
-  // column sums of P.
-  static constexpr int kVS = 128 * 128 * 2;
+  static constexpr int kKV = 128 * D * 2;            // one K tile (and one V tile)
+  // The PV MMA's A operand (V^T) always spans 128 head dimensions: at
+  // head_dim 64 it keeps M = 128, and its upper half is one region shared by
+  // every V slot (the descriptor's leading byte offset points there), written
+  // once: all zeros except dimension 64, which holds ones so that O^T row 64
+  // accumulates the column sums of P.
+  static constexpr int kVS = kKV;
   static constexpr bool kOnesRow = D == 64;
+  static constexpr int kOnes = kOnesRow ? 16384 : 0;
   static constexpr int kQ = kHalves * NQP * 128;     // Q^T operand [half][NQP][128 B]
   static constexpr int kP = 2 * NQP * 128;           // P^T operand [kblock][NQP][128 B]
   static constexpr int kThreads = 384;               // 12 warps
   static constexpr int kCol = NQP < 32 ? 32 : NQP;   // tensor-memory columns per accumulator
   static constexpr uint32_t kTmemCols = 4 * kCol;    // S0, S1, O0, O1
   static constexpr int kOffV = KS * kKV;
-  static constexpr int kOffQ = kOffV + VS * kVS;
+  static constexpr int kOffOnes = kOffV + VS * kVS;  // 1024-byte aligned, like every tile
+  static constexpr int kOffQ = kOffOnes + kOnes;
   static constexpr int kOffP = kOffQ + kQ;
   static constexpr int kOffBar = kOffP + 2 * kP;
   static constexpr int kNumBars = 2 * KS + 2 * VS + 4 * 2 + 1;
@@ -245,13 +252,13 @@ __global__ void __launch_bounds__(384, 1)
             qreg[u];
     }
     if constexpr (Cfg::kOnesRow) {
-      // the upper half of every V slot: zeros, and ones at head dimension 64
+      // the shared upper half of V^T: zeros, and ones at head dimension 64
       // (element (pos, 64) of the MN-major swizzled half sits at chunk pos % 8)
-      for (int e = st; e < VS * 128 * 8; e += SN) {
-        const int sl = e / (128 * 8), pos = (e / 8) % 128, ch = e % 8;
+      for (int e = st; e < 128 * 8; e += SN) {
+        const int pos = e / 8, ch = e % 8;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (ch == (pos & 7)) v.x = 0x3F80u;   // bf16 1.0 in the chunk's first element
-        *reinterpret_cast<uint4*>(smem + Cfg::kOffV + sl * Cfg::kVS + 16384 + pos * 128 + ch * 16) = v;
+        *reinterpret_cast<uint4*>(smem + Cfg::kOffOnes + pos * 128 + ch * 16) = v;
       }
     }
     for (int n = st; n < NQP; n += SN) {
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(384, 1)
     // holds (address / 16) mod 2^14, the part of a shared-window address the
     // tensor cores use, so it is added and masked last.
     const uint64_t dSw = smem_desc(0, 16, 1024, 2);       // K-major, 128-byte swizzle
-    const uint64_t dVmn = smem_desc(0, 16384, 1024, 2);   // V as the MN-major A operand
+    const uint64_t dVmn = smem_desc(0, 16384, 1024, 2);   // MN-major operand, halves 16 KB apart
     auto with_addr = [](uint64_t d, uint32_t a16) { return d | uint64_t(a16 & 0x3FFFu); };
     const uint32_t qb = (sbase + Cfg::kOffQ) >> 4;
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
@@ -385,10 +392,15 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const uint32_t vb = (sbase + Cfg::kOffV + s * Cfg::kVS) >> 4;
       const uint32_t pb = (sbase + Cfg::kOffP + gg * Cfg::kP) >> 4;
+      // V^T as the MN-major A operand; at head_dim 64 its upper half is the
+      // shared ones region, one leading byte offset past the slot
+      const uint64_t dV =
+          Cfg::kOnesRow ? smem_desc(0, uint32_t(Cfg::kOffOnes - Cfg::kOffV - s * Cfg::kVS), 1024, 2)
+                        : dVmn;
       if (leader) {
 #pragma unroll
         for (int kp = 0; kp < 8; ++kp)
-          tc_mma(tmem + 2 * kCol + kCol * gg, with_addr(dVmn, vb + kp * 128),
+          tc_mma(tmem + 2 * kCol + kCol * gg, with_addr(dV, vb + kp * 128),
                  kPmn ? with_addr(dVmn, pb + kp * 128)
                       : with_addr(dSw, pb + (kp >> 2) * (NQP * 8) + (kp & 3) * 2),
                  idPV, t >= 2 || kp > 0);
