@@ -55,15 +55,16 @@ def read_peaks():
 
 
 # DRAM traffic of one verify launch (dram__bytes_read.sum + dram__bytes_write.sum)
-# on this workload, from a one-pass ncu capture of the verify launches of
-# `python bench.py --steps 8 --warmup 3 --no-cpu-baseline`; reported only while
+# on this workload, from a one-pass ncu capture of five consecutive verify
+# launches of `python bench.py --profile --steps 8 --warmup 3` (134.42 MB read,
+# 0.47-0.86 MB written per launch); reported only while
 # the kernel sources still hash to the digest they had when the counters were
 # taken.
 VERIFY_TRAFFIC = {
-    "bytes": 134_800_000,
+    "bytes": 135_100_000,
     "sources": ["verify_tc.cu", "split_merge.cuh", "attn_core.cuh", "vegas_common.cuh",
                 "kernels.h"],
-    "sha256": "1f65197358ad7fb2ad22940dd40f7d1ca0f86fde912b9f377bc2825212467b00",
+    "sha256": "7ba1d611912705287edc8d79d1bea87b4f8f9db295b21966421957a8d39148f8",
 }
 
 
