@@ -178,16 +178,32 @@ __device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
   const int hl2 = __ffs(__ballot_sync(0xffffffffu, hit2)) - 1;
   const int bin = sb * kFine + (kFine - 1 - hl2);
   const uint32_t above_bin = above + __shfl_sync(0xffffffffu, fexcl, hl2);
-  // per CTA: keys in bins above the chosen one, and inside it
+  // per CTA: keys in bins above the chosen one (summed over the lanes by a
+  // reduce-scatter: lane 4q ends with CTA q's sum), and inside it
+  uint32_t up[kMaxSelCluster];
 #pragma unroll
-  for (int q = 0; q < kMaxSelCluster; ++q) {
-    const uint32_t up = (sbh > sb ? ch[q] : 0u) + (sbl > sb ? cl[q] : 0u) + (lane < hl2 ? f[q] : 0u);
-    const uint32_t gtq = warp_sum(up);
-    const uint32_t inq = __shfl_sync(0xffffffffu, f[q], hl2);
-    if (lane == 0 && q < CL) {
-      st.gt[q] += gtq;
-      st.in[q] = inq;
+  for (int q = 0; q < kMaxSelCluster; ++q)
+    up[q] = (sbh > sb ? ch[q] : 0u) + (sbl > sb ? cl[q] : 0u) + (lane < hl2 ? f[q] : 0u);
+  static_assert(kMaxSelCluster == 8, "three halving rounds");
+#pragma unroll
+  for (int r = 0, w = kMaxSelCluster / 2; w >= 1; ++r, w >>= 1) {
+    const bool hi = lane & (16 >> r);   // keeps the upper w of the 2w values held
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const uint32_t send = hi ? up[j] : up[j + w];
+      up[j] = (hi ? up[j + w] : up[j]) + __shfl_xor_sync(0xffffffffu, send, 16 >> r);
     }
+  }
+  up[0] += __shfl_xor_sync(0xffffffffu, up[0], 2);
+  up[0] += __shfl_xor_sync(0xffffffffu, up[0], 1);
+  uint32_t inq[kMaxSelCluster];
+#pragma unroll
+  for (int q = 0; q < kMaxSelCluster; ++q) inq[q] = __shfl_sync(0xffffffffu, f[q], hl2);
+  if ((lane & 3) == 0 && (lane >> 2) < CL) st.gt[lane >> 2] += up[0];
+  if (lane < CL) {
+#pragma unroll
+    for (int q = 0; q < kMaxSelCluster; ++q)
+      if (q == lane) st.in[q] = inq[q];
   }
   // key bounds of the chosen bin over the cluster (held by lane hl2)
   uint32_t a = 0xffffffffu, z = 0u;
@@ -210,7 +226,7 @@ __device__ __forceinline__ void search_level(cg::cluster_group& cluster, int CL,
 // sequence from the sum over its KV heads.
 template <int P, bool SHARED>
 __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelectParams p) {
-  griddep_begin();
+  griddep_launch_dependents();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
@@ -227,6 +243,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   __shared__ uint32_t red[2 * kSelWarps];
   __shared__ uint32_t xch[2 * kMaxSelCluster];   // every CTA's key range, pushed here
   __shared__ SelState st;
+  // Both histogram sets are cleared before the wait for the previous kernel
+  // (no global memory is touched before it).
+  for (int i = tid; i < 2 * kBins; i += kSelThreads) {
+    cnt[i] = 0u;
+    bmn[i] = 0xffffffffu;
+    bmx[i] = 0u;
+  }
+  if (tid < kMaxSelCluster) {
+    st.gt[tid] = 0u;
+    st.in[tid] = 0u;
+  }
+  griddep_wait();
 
   // Warp w owns chunk offsets r = 32 P w + 32 u + lane, u < P: contiguous per
   // warp, so position order is (rank, warp, u, lane).  The first keys are
@@ -270,15 +298,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   }
   const int nvalid = max(0, min(p.chunk, L - start));
 
-  for (int i = tid; i < 2 * kBins; i += kSelThreads) {
-    cnt[i] = 0u;
-    bmn[i] = 0xffffffffu;
-    bmx[i] = 0u;
-  }
-  if (tid < kMaxSelCluster) {
-    st.gt[tid] = 0u;
-    st.in[tid] = 0u;
-  }
+  // At eight keys a thread the keys stay in registers; larger chunks keep
+  // them in shared memory.
+  constexpr bool kRegKeys = P <= 8;
+  uint32_t kreg[kRegKeys ? P : 1];
+#pragma unroll
+  for (int u = 0; u < (kRegKeys ? P : 1); ++u) kreg[u] = 0u;
+  auto key_at = [&](int u, int r) {
+    if constexpr (kRegKeys)
+      return kreg[u];
+    else
+      return keys[r];
+  };
   uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll 1
   for (int u0 = 0; u0 < P; u0 += 8) {
@@ -294,7 +325,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
       const int r = r0 + (u0 + i) * 32;
       if (r < nvalid) {
         const uint32_t key = order_key(v[i]);
-        keys[r] = key;
+        if constexpr (kRegKeys)
+          kreg[u0 + i] = key;
+        else
+          keys[r] = key;
         kmin = min(kmin, key);
         kmax = max(kmax, key);
       }
@@ -356,7 +390,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     for (int u = 0; u < P; ++u) {
       const int r = r0 + u * 32;
       if (r >= nvalid) continue;
-      const uint32_t key = keys[r];
+      const uint32_t key = key_at(u, r);
       uint32_t d;
       if (mode == kKeyBits) {
         if (key < klo || key > khi) continue;
@@ -378,13 +412,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
       atomicMax(&mx[d], key);
     }
     __syncthreads();
-    // super-bin sums: warp w adds super-bins 4w .. 4w + 3 and pushes each
-    // into every CTA's su[rank][.] (lane q -> CTA q)
-#pragma unroll
-    for (int j = 0; j < kSuper / kSelWarps; ++j) {
-      const int sb = (kSuper / kSelWarps) * warp + j;
-      const uint32_t x = warp_sum(c[sb * kFine + lane]);
-      if (lane < CL) cluster.map_shared_rank(su, lane)[rank * kSuper + sb] = x;
+    // super-bin sums: thread t adds bins 4t .. 4t + 3, the eight threads of a
+    // super-bin reduce with shuffles, and the first pushes the sum into every
+    // CTA's su[rank][.]
+    static_assert(4 * kSelThreads == kBins && kFine == 32, "four bins a thread");
+    {
+      const uint4 c4 = *reinterpret_cast<const uint4*>(c + 4 * tid);
+      uint32_t x = c4.x + c4.y + c4.z + c4.w;
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      if ((tid & 7) == 0)
+        for (int q = 0; q < CL; ++q) cluster.map_shared_rank(su, q)[rank * kSuper + (tid >> 3)] = x;
     }
     cluster.sync();
     // The other set's last readers (the previous level's search) are past
@@ -425,7 +464,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
     const bool valid = r < nvalid;
-    const uint32_t key = valid ? keys[r] : 0u;
+    const uint32_t key = valid ? key_at(u, r) : 0u;
     n_gt += __popc(__ballot_sync(0xffffffffu, valid && key > tau));
     n_eq += __popc(__ballot_sync(0xffffffffu, valid && key == tau));
   }
@@ -452,7 +491,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   for (int u = 0; u < P; ++u) {
     const int r = r0 + u * 32;
     const bool valid = r < nvalid;
-    const uint32_t key = valid ? keys[r] : 0u;
+    const uint32_t key = valid ? key_at(u, r) : 0u;
     const bool is_gt = valid && key > tau, is_eq = valid && key == tau;
     const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
     const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
