@@ -58,6 +58,12 @@ constexpr int kMaxSelCluster = 8;
 // two sets (one per level parity) of {count, min key, max key} per bin, and of
 // every CTA's super-bin counts
 constexpr int kLevelWords = 6 * kBins + 2 * kMaxSelCluster * kSuper;
+// With more than eight keys a thread, a chosen value bin holding at most this
+// many keys over the cluster is resolved from its keys directly instead of by
+// a second histogram level.  (At eight keys a thread the extra code measured
+// slower than the second level it saves.)
+constexpr int kMaxCand = 256;
+constexpr int kCandWords = kMaxCand + 4;   // the keys, then count, tau, keys above tau
 
 // Binning of a level: value bins of [min, max] (counts only), sub-bins of the
 // chosen value bin, bits of key - klo; kDone once [klo, khi] holds one key.
@@ -240,6 +246,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   uint32_t* bmx = smem + 4 * kBins;        // [2][kBins] largest key of each bin
   uint32_t* sup = smem + 6 * kBins;        // [2][kMaxSelCluster][kSuper] every CTA's super-bin counts
   uint32_t* keys = smem + kLevelWords;     // [chunk]
+  // (P > 8) keys of the chosen value bin, by CTA; then count, tau, keys above tau
+  uint32_t* cand = keys + p.chunk;
   __shared__ uint32_t red[2 * kSelWarps];
   __shared__ uint32_t xch[2 * kMaxSelCluster];   // every CTA's key range, pushed here
   __shared__ SelState st;
@@ -253,6 +261,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   if (tid < kMaxSelCluster) {
     st.gt[tid] = 0u;
     st.in[tid] = 0u;
+  }
+  if constexpr (P > 8) {
+    if (tid < 4) cand[kMaxCand + tid] = 0u;
   }
   griddep_wait();
 
@@ -442,6 +453,69 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     if (mode == kValueBins) {
       vbin = st.bin;
       mode = kSubBins;
+      uint32_t nb = 0, base = 0;   // keys in the chosen bin: all, and in the CTAs before this one
+      for (int q = 0; q < CL; ++q) {
+        nb += st.in[q];
+        base += q < rank ? st.in[q] : 0u;
+      }
+      if (P > 8 && nb <= (uint32_t)kMaxCand) {
+        uint32_t& ncand = cand[kMaxCand];
+        uint32_t& cand_tau = cand[kMaxCand + 1];
+        uint32_t& cand_above = cand[kMaxCand + 2];
+        // Few keys in the chosen bin: every CTA pushes its keys of the bin
+        // into every CTA's cand[] (CTA q's at the bin counts of the CTAs
+        // before it), and each CTA finds tau, the need-th largest of them,
+        // and the per-CTA counts above and at tau, locally.
+#pragma unroll 8
+        for (int u = 0; u < P; ++u) {
+          const int r = r0 + u * 32;
+          if (r >= nvalid) continue;
+          const uint32_t key = key_at(u, r);
+          const float t = __fmul_rn(__fsub_rn(key_value(key), vmin), scale);
+          const uint32_t bin = min((uint32_t)kBins - 1u, __float2uint_rz(fmaxf(0.f, t)));
+          if (bin != vbin) continue;
+          const uint32_t j = base + atomicAdd(&ncand, 1u);
+          if (j < (uint32_t)kMaxCand)   // always (the bin counts bound it)
+            for (int q = 0; q < CL; ++q) cluster.map_shared_rank(cand, q)[j] = key;
+        }
+        cluster.sync();
+        for (uint32_t t = tid; t < nb; t += kSelThreads) {
+          const uint32_t kt = cand[t];
+          uint32_t n_gt = 0, n_ge = 0;
+          for (uint32_t j = 0; j < nb; ++j) {
+            n_gt += cand[j] > kt ? 1u : 0u;
+            n_ge += cand[j] >= kt ? 1u : 0u;
+          }
+          if (n_gt < need && need <= n_ge) {   // every such thread holds the same key
+            cand_tau = kt;
+            cand_above = n_gt;
+          }
+        }
+        __syncthreads();
+        const uint32_t tau_c = cand_tau;
+        if (warp == 0) {
+          // lane q < CL: CTA q's segment cand[b0, b0 + in[q])
+          uint32_t b0 = 0, nq = 0;
+          for (int q = 0; q < CL; ++q) {
+            b0 += q < lane ? st.in[q] : 0u;
+            nq = q == lane ? st.in[q] : nq;
+          }
+          __syncwarp();
+          uint32_t a = 0, e = 0;
+          for (uint32_t j = b0; j < b0 + nq; ++j) {
+            a += cand[j] > tau_c ? 1u : 0u;
+            e += cand[j] == tau_c ? 1u : 0u;
+          }
+          if (lane < CL) {
+            st.gt[lane] += a;
+            st.in[lane] = e;
+          }
+        }
+        __syncthreads();
+        need -= cand_above;
+        klo = khi = tau_c;
+        mode = kDone;
+      }
     } else {
       klo = st.klo;
       khi = st.khi;
@@ -505,7 +579,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
   cluster_wait();     // no CTA leaves while another may still read its shared memory
 }
 
-size_t select_smem_bytes(int chunk) { return size_t(kLevelWords + chunk) * 4; }
+size_t select_smem_bytes(int chunk) {
+  return size_t(kLevelWords + chunk + (chunk > 8 * kSelThreads ? kCandWords : 0)) * 4;
+}
 
 template <int P, bool SHARED>
 static cudaError_t launch_select_p(const SelectParams& p, int cluster, int batch,
