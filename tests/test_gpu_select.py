@@ -44,6 +44,16 @@ def test_select_heavy_ties_and_signed_zero():
     _run(s, [50000], [777], 800)
 
 
+@pytest.mark.parametrize("L,k", [(65536, 3277), (131072, 100)])
+def test_select_ties_inside_the_chosen_bin(L, k):
+    """About 64 equal keys per value, so the chosen value bin holds one tied
+    group small enough to be resolved from its keys directly (wide chunks);
+    ties go to the lower position."""
+    rng = np.random.default_rng(L + 7)
+    s = (rng.integers(0, L // 64, size=(2, 3, L)) * 0.25).astype(np.float32)
+    _run(s, [L, L], [k, k], k + 5)
+
+
 def test_select_variable_lengths_and_k():
     rng = np.random.default_rng(2)
     lens = [10, 40000, 3, 20001]
