@@ -33,6 +33,8 @@ SMALL = {
     "cluster3_ragged": C2.with_(ctx_lo=400, ctx_hi=400),                   # 3 splits of 9, 9, 8 pages
     "qwen_b2_mixed": C3.with_(batch=2, ctx_lo=150, ctx_hi=6000),           # one short, one long
     "tc_ticket_b13": C3.with_(batch=13, ctx_lo=600, ctx_hi=900),           # 104 units: workspace merge
+    "gptoss_b5_ragged": C4.with_(batch=5, ctx_lo=3000, ctx_hi=9000),      # 40 units, 3-CTA clusters
+    "gptoss_b3_short": C4.with_(batch=3, ctx_lo=1, ctx_hi=700),           # a few tiles a unit
 }
 
 
