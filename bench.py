@@ -196,17 +196,34 @@ class GpuIteration:
                               for r in range(replicas)]))
         self.kv = [vg.paged_kv(self.k, self.v, self.bt[r], w.hq) for r in range(replicas)]
         bf = lambda a: t(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
-        self.qv = bf(gen.f32_to_bf16_bits(gen.verify_queries_f32(w)))
-        self.qd = bf(gen.f32_to_bf16_bits(gen.draft_queries_f32(w)))
+
+        def packed(specs):
+            """One device allocation holding tensors of the given (shape, dtype),
+            each at a 256-byte boundary, so a step's inputs (and its outputs)
+            move between host and device in one copy."""
+            sizes = [int(np.prod(sh)) * torch.empty(0, dtype=dt).element_size() for sh, dt in specs]
+            offs = [0]
+            for n in sizes:
+                offs.append(offs[-1] + (n + 255) // 256 * 256)
+            buf = torch.empty(offs[-1], dtype=torch.uint8, device=dev)
+            return buf, [buf[offs[i]:offs[i] + sizes[i]].view(dt).view(sh)
+                         for i, (sh, dt) in enumerate(specs)]
+
+        qv0 = bf(gen.f32_to_bf16_bits(gen.verify_queries_f32(w)))
+        qd0 = bf(gen.f32_to_bf16_bits(gen.draft_queries_f32(w)))
+        self.io_in, (self.qv, self.qd) = packed([(tuple(qv0.shape), torch.bfloat16),
+                                                 (tuple(qd0.shape), torch.bfloat16)])
+        self.qv.copy_(qv0)
+        self.qd.copy_(qd0)
         self.lens_t, self.kps_t = lens_t, t(self.kps)
         self.stride = int(self.lens.max())
         self.k_max = int(self.kps.max())
         self.tails = [gen.tail_len(w, j) for j in range(w.gamma)]
         self.tl_t = [torch.full((w.batch,), tl, dtype=torch.int32, device=dev) for tl in self.tails]
-        self.out_v = torch.empty_like(self.qv)
-        self.out_d = torch.empty_like(self.qd)
+        self.io_out, (self.out_v, self.out_d, self.idx) = packed(
+            [(tuple(self.qv.shape), torch.bfloat16), (tuple(self.qd.shape), torch.bfloat16),
+             ((w.batch, w.hkv, self.k_max), torch.int32)])
         self.scores = torch.empty((w.batch, w.hkv, self.stride), dtype=torch.float32, device=dev)
-        self.idx = torch.empty((w.batch, w.hkv, self.k_max), dtype=torch.int32, device=dev)
         self.kw_t = torch.zeros((w.batch,), dtype=torch.int32, device=dev)
         # the pages' capture: raw logits of rows {0, gamma} of every query head
         self.raw_rows = len({0, w.gamma})
@@ -745,28 +762,25 @@ def run_e2e(it, stream, steps, nbytes):
     its queries from pinned host memory, runs the iteration, and reads back the
     verify outputs, the draft outputs and the selected indices."""
     torch = it.torch
-    pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)  # noqa: E731
-    qv_h, qd_h = pin(it.qv), pin(it.qd)
-    qv_h.copy_(it.qv.cpu())
-    qd_h.copy_(it.qd.cpu())
-    ov_h, od_h, idx_h = pin(it.out_v), pin(it.out_d), pin(it.idx)
-    # One graph per KV replica holds the whole step: the host-to-device copies
-    # of the step's queries, the iteration, and the device-to-host copies of
-    # its outputs (all pinned host memory), so a step costs the host one
-    # launch and one synchronisation.
+    # the step's queries (verify and draft) and its outputs (verify and draft
+    # outputs, selected indices) each sit in one packed device buffer
+    in_h = torch.empty(it.io_in.shape, dtype=torch.uint8, pin_memory=True)
+    in_h.copy_(it.io_in.cpu())
+    out_h = torch.empty(it.io_out.shape, dtype=torch.uint8, pin_memory=True)
+    # One graph per KV replica holds the whole step: the host-to-device copy
+    # of the step's queries, the iteration, and the device-to-host copy of its
+    # outputs (pinned host memory), so a step costs the host one launch and
+    # one synchronisation.
     graphs = []
     for r in range(it.R):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            it.qv.copy_(qv_h, non_blocking=True)
-            it.qd.copy_(qd_h, non_blocking=True)
+            it.io_in.copy_(in_h, non_blocking=True)
             it.step(r)
-            ov_h.copy_(it.out_v, non_blocking=True)
-            od_h.copy_(it.out_d, non_blocking=True)
-            idx_h.copy_(it.idx, non_blocking=True)
+            out_h.copy_(it.io_out, non_blocking=True)
         graphs.append(g)
-    bi = qv_h.numel() * 2 + qd_h.numel() * 2
-    bo = ov_h.numel() * 2 + od_h.numel() * 2 + idx_h.numel() * 4
+    bi = in_h.numel()
+    bo = out_h.numel()
 
     def one(i):
         with torch.cuda.stream(stream):
