@@ -445,6 +445,7 @@ def time_variants(it, stream, reps=100):
         "aggregate_raw_logits_us": lambda i: it.aggregate_raw(),
         "paper_style_capture_us": lambda i: (it.verify_raw(i % it.R), it.aggregate_raw()),
         "select_us": lambda i: it.select(),
+        "draft_step_us": lambda i: it.draft(i % it.R, i % w.gamma),
         "select_shared_us": lambda i: it.select_shared(),
         "select_window_us": lambda i: it.select_window(),
         "iteration_window_selector_us": lambda i: it.window_step(i % it.R),
@@ -736,8 +737,9 @@ def run_gpu(args, rank, world, dist, peak, peak_kind):
         vb = per_call_us(torch, stream, lambda i: it.verify(i % it.R), 4 * it.R)
         vp = per_call_us(torch, stream, lambda i: it.verify(i % it.R, capture=False), 4 * it.R)
         sl = per_call_us(torch, stream, lambda i: it.select(), 8)
+        dr = per_call_us(torch, stream, lambda i: it.draft(i % it.R, i % w.gamma), 8)
         variants = {"verify_capture2_us": round(vb, 3), "verify_no_capture_us": round(vp, 3),
-                    "select_us": round(sl, 3)}
+                    "select_us": round(sl, 3), "draft_step_us": round(dr, 3)}
         e2e = None
         return (it, nbytes, ms_step, K_eff, stages, timing, clocks, e2e, variants, {})
     e2e = run_e2e(it, stream, min(K_eff, 500), nbytes)
@@ -1032,11 +1034,17 @@ def main():
                                 "timed back to back in a graph of its own launches")
     line["roofline"] = roofline_entry(nbytes["verify"], vb2b, peak, peak_kind, v_us,
                                       kernel=verify_kernel_name(w))
+    # the draft kernel, the same way: per launch back to back, stage events as context
+    d_b2b, d_st = variants["draft_step_us"], stages["draft_us_per_step"]
+    d_bytes = int(round(statistics.mean(nbytes["draft"])))   # the steps' mean (their tails differ)
     line["roofline_draft"] = {
-        "kernel": "sparse_decode_kernel", "bound": "hbm", "bytes_per_launch": nbytes["draft"][-1],
-        "duration_us": round(stages["draft_us_per_step"], 3),
-        "frac": round(nbytes["draft"][-1] / (stages["draft_us_per_step"] * 1e-6) / 1e9 / peak, 4),
-        "duration_source": "stage events around the draft steps, per step"}
+        "kernel": "sparse_decode_kernel", "bound": "hbm", "bytes_per_launch": d_bytes,
+        "duration_us": round(d_b2b, 3),
+        "frac": round(d_bytes / (d_b2b * 1e-6) / 1e9 / peak, 4),
+        "duration_source": "CUDA events around a graph of back-to-back draft steps (rotating "
+                           "the KV replicas and the step index) on the launching stream, per step",
+        "stage_events": {"duration_us": round(d_st, 3),
+                         "frac": round(d_bytes / (d_st * 1e-6) / 1e9 / peak, 4)}}
     # the "next" rows, measured the same way on the same workload: collect-all
     # capture, one T shared by all heads, the query-agnostic window selector
     line["variants"] = variants
