@@ -64,7 +64,7 @@ VERIFY_TRAFFIC = {
     "bytes": 135_100_000,
     "sources": ["verify_tc.cu", "split_merge.cuh", "attn_core.cuh", "vegas_common.cuh",
                 "kernels.h"],
-    "sha256": "7ba1d611912705287edc8d79d1bea87b4f8f9db295b21966421957a8d39148f8",
+    "sha256": "a3f69b7ee626b449718abd19bdce9a340773a941953e9fc0c4cc69de9cd85269",
 }
 
 

@@ -6,18 +6,21 @@
 // Self-Speculative Decoding with Verification-Guided Sparse Attention",
 // gist.science technical summary, §2 "Core mechanism", §2.A, §2.B
 // "Collect-2-Query", §3 "Implementation"), used when the unit's query columns
-// (the (gamma+1)*G rows plus the two capture columns) fit in 32.
+// (the (gamma+1)*G rows plus the two capture columns) fit in 40 at head_dim
+// 128 and 64 at head_dim 64.
 //
 // One CTA per (split, KV head, sequence), 12 warps:
-//   warps 0, 10, 11  TMA producers (issue rate is per warp, so a tile's 32
-//              boxes are spread over three warps): K and V tiles of 128
-//              positions (8 pages) stream into 3-slot K and V rings, block-table
-//              entries prefetched four tiles ahead;
+//   warps 0, 10, 11  TMA producers (issue rate is per warp, so a tile's boxes
+//              are spread over three warps): K and V tiles of 128 positions (8
+//              pages) stream into K and V rings (3 + 3 slots; 3 + 4 at head_dim
+//              64), block-table entries prefetched four tiles ahead;
 //   warp 1     allocates tensor memory; the warp runs the MMA loop uniformly
 //              and one elected lane issues
-//                S^T[128 pos x N] = K[128 x 128] . Q^T   (both K-major, the K
+//                S^T[128 pos x N] = K[128 x D] . Q^T   (both K-major, the K
 //                tile consumed straight from the TMA's 128-byte swizzle),
-//                O^T[128 d x N]  += V^T[128 x 128] . P^T (V read MN-major);
+//                O^T[128 d x N]  += V^T[128 x 128] . P^T (V read MN-major; at
+//                head_dim 64 the upper half of V^T is one shared region of
+//                zeros with a ones row, so O^T row 64 sums P);
 //   warps 2-5  softmax group 0 (even tiles), warps 6-9 group 1 (odd tiles):
 //              thread i of a group owns tensor-memory lane i, i.e. tile
 //              position i for S and head dimension i for its O^T accumulator.
@@ -27,8 +30,10 @@
 // two capture columns hold the summed captured query, so the score is their
 // sum), masks, and raises the running maxima only when a logit exceeds them by
 // 8 (one vote per group); only then is the group's O^T rescaled in tensor
-// memory.  It writes P^T = 2^(x - m) as bf16 into a 128-byte-swizzled shared
-// buffer that the PV MMA reads.
+// memory.  It writes P^T = 2^(x - m) as bf16 (wide tiles: 2^y with y taken
+// relative to a per-column reference in one FMA) into a 128-byte-swizzled
+// shared buffer that the PV MMA reads (K-major up to 32 columns, MN-major for
+// 64-column tiles).
 //
 // Splits of a unit merge either on chip, when all of them form one
 // thread-block cluster (every group pushes its state to the rank that owns the
