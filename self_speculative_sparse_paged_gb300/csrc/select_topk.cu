@@ -19,7 +19,10 @@
 //           below the span's top bit.
 // From level 1 on, every bin also records its smallest and largest key, so
 // the chosen bin gives the next [klo, khi] exactly and the search ends as soon
-// as that interval holds one key value (usually after level 1).
+// as that interval holds one key value (usually after level 1).  With more
+// than eight keys a thread, a level-0 bin holding at most 256 keys over the
+// cluster is resolved without level 1: every CTA sends its keys of the bin to
+// every CTA, and each CTA ranks them locally.
 //
 // Each CTA also sums its histogram into 64 super-bins of 32 bins and pushes
 // them (and, once, its key range) into every CTA of the cluster with remote
