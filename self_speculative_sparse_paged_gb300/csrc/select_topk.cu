@@ -88,8 +88,11 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 constexpr uint32_t kKeyNegInf = 0x007fffffu;   // order_key(-inf)
 constexpr uint32_t kKeyPosInf = 0xff800000u;   // order_key(+inf)
 
+// First half of the exit barrier: this CTA reads no other CTA's shared memory
+// from here on.  Every remote read before it has already been consumed, so
+// the arrival publishes nothing and needs no release ordering.
 __device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
