@@ -1025,7 +1025,7 @@ def main():
             "e2e": e2e}
     v_us = stages["verify_us"]
     line["stages"] = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in stages.items()}
-    # §8: capture plus top-k over plain verify, back to back (each kernel in a
+    # the capture-plus-top-k overhead over plain verify, back to back (each kernel in a
     # graph of its own launches), and over the stage events
     vb2b, vplain = variants["verify_capture2_us"], variants["verify_no_capture_us"]
     line["capture_plus_select_overhead"] = round((vb2b + variants["select_us"]) / vplain - 1.0, 4)

@@ -55,7 +55,7 @@ extern "C" {
 typedef enum {
   VEGAS_OK = 0,
   VEGAS_ERR_INVALID_ARG = 1,         /* host-side argument check failed; nothing launched */
-  VEGAS_ERR_UNSUPPORTED = 2,         /* valid but outside this build's supported shapes */
+  VEGAS_ERR_UNSUPPORTED = 2,         /* valid but outside the shapes this library supports */
   VEGAS_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the *_workspace_size() value */
   VEGAS_ERR_CUDA = 4,                /* a CUDA runtime call failed (see detail string) */
   VEGAS_ERR_DEVICE_FAULT = 5,        /* a kernel met an out-of-range page, index or k */
