@@ -269,6 +269,25 @@ class GpuIteration:
         self.vg.vegas_select_topk_shared(self.scores, self.stride, self.lens_t, self.kps_t,
                                          self.idx, w.batch, w.hkv, self.k_max)
 
+    def select_outliers(self):
+        """The select on a copy of the captured scores in which eight positions
+        of every (sequence, KV head) row carry a logit a thousand times the
+        row's largest magnitude: a few outliers stretch the row's [min, max]
+        (real logits are not bounded like the synthetic ones)."""
+        w, torch = self.w, self.torch
+        if getattr(self, "scores_out", None) is None:
+            rng = np.random.default_rng(w.seed + 11)
+            self.scores_out = self.scores.clone()
+            for b in range(w.batch):
+                L = int(self.lens[b])
+                for g in range(w.hkv):
+                    row = self.scores_out[b, g, :L]
+                    pos = torch.from_numpy(rng.choice(L, size=min(8, L), replace=False)).to(self.dev)
+                    row[pos] = 1000.0 * float(row.abs().max().item()) * (1.0 + torch.arange(
+                        len(pos), device=self.dev, dtype=torch.float32) / 16)
+        self.vg.vegas_select_topk(self.scores_out, self.stride, self.lens_t, self.kps_t, self.idx,
+                                  w.batch, w.hkv, self.k_max)
+
     def select_window(self):
         w = self.w
         # as many positions as the verification-guided selector keeps: sinks + window
@@ -445,6 +464,7 @@ def time_variants(it, stream, reps=100):
         "aggregate_raw_logits_us": lambda i: it.aggregate_raw(),
         "paper_style_capture_us": lambda i: (it.verify_raw(i % it.R), it.aggregate_raw()),
         "select_us": lambda i: it.select(),
+        "select_with_outliers_us": lambda i: it.select_outliers(),
         "draft_step_us": lambda i: it.draft(i % it.R, i % w.gamma),
         "select_shared_us": lambda i: it.select_shared(),
         "select_window_us": lambda i: it.select_window(),

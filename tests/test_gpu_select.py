@@ -69,6 +69,20 @@ def test_select_clustered_values():
     _run(s, [32768], [1639], 1639)
 
 
+@pytest.mark.parametrize("L,k", [(32768, 1639), (131072, 3933)])
+def test_select_with_large_outliers(L, k):
+    """A few logits a thousand times above (and below) the rest stretch the
+    row's [min, max]: level 0's value bins then hold the bulk in one bin, and
+    the search goes on by sub-bins and key bits."""
+    rng = np.random.default_rng(L + 9)
+    s = (rng.standard_normal((1, 4, L)) * 3).astype(np.float32)
+    for h in range(4):
+        pos = rng.choice(L, size=16, replace=False)
+        s[0, h, pos[:8]] = 3000.0 * (1 + np.arange(8) / 16)
+        s[0, h, pos[8:]] = -3000.0 * (1 + np.arange(8) / 16)
+    _run(s, [L], [k], k + 3)
+
+
 # ---------------------------------------------------------------- shared T (all heads)
 def _run_shared(scores32: np.ndarray, lens, kps, k_max):
     B, H, S = scores32.shape
