@@ -27,11 +27,13 @@ namespace cg = cooperative_groups;
 
 namespace vegas {
 
-template <int D>
+template <int D, int NT>
 struct SparseCfg {
-  // 16-row groups in flight per warp: a head_dim-64 group is half the bytes of
-  // a head_dim-128 one, so it keeps twice as many in flight
-  static constexpr int kStages = D == 64 ? 4 : 2;
+  // 16-row groups in flight per warp: four at head_dim 64 (a group is half
+  // the bytes of a head_dim-128 one), three at head_dim 128 with one column
+  // tile (measured 1-2% faster than two), two with two column tiles (three do
+  // not fit the shared memory there)
+  static constexpr int kStages = D == 64 ? 4 : (NT == 1 ? 3 : 2);
   static constexpr int kRow = D * 2 + 16;           // padded row stride
   static constexpr int kTile = 16 * kRow;
   static constexpr int kStage = 2 * kTile;
@@ -41,25 +43,31 @@ struct SparseCfg {
 
 template <int D, int NT>
 constexpr size_t sparse_smem_layout_bytes() {
-  return SparseCfg<D>::kStageBytes                                 // stages
+  using Cfg = SparseCfg<D, NT>;
+  return Cfg::kStageBytes                                          // stages
          + size_t(NT) * 8 * (2 * D + 16)                           // Q tile
-         + (size_t(kAttnWarps) * SparseCfg<D>::kStages + 1) * 8    // mbarriers (+ receive)
-         + size_t(SparseCfg<D>::kMaxRows) * 4                      // row table
+         + (size_t(kAttnWarps) * Cfg::kStages + 1) * 8             // mbarriers (+ receive)
+         + size_t(Cfg::kMaxRows) * 4                               // row table
          + size_t(NT) * 8 * (D + 2) * 4                            // CTA partial
-         + (size_t(NT) * 8 * D + kMaxSparseCluster) * 4              // received output slices
-         + size_t(kMaxSparseCluster) * NT * 8 * 2 * 4                // received m, l
+         + (size_t(NT) * 8 * D + kMaxSparseCluster) * 4            // received output slices
+         + size_t(kMaxSparseCluster) * NT * 8 * 2 * 4              // received m, l
          + 1024;
 }
+static_assert(sparse_smem_layout_bytes<128, 1>() <= 227 * 1024 &&
+                  sparse_smem_layout_bytes<128, 2>() <= 227 * 1024 &&
+                  sparse_smem_layout_bytes<64, 1>() <= 227 * 1024 &&
+                  sparse_smem_layout_bytes<64, 2>() <= 227 * 1024,
+              "shared memory of a draft CTA");
 
 template <int D, int NT>
 __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const SparseParams p) {
   constexpr int W = kAttnWarps;
   constexpr int NTH = W * 32;
   constexpr int NPAD = NT * 8;
-  constexpr int STAGES = SparseCfg<D>::kStages;
-  constexpr int ROW = SparseCfg<D>::kRow;
-  constexpr int TILE = SparseCfg<D>::kTile;
-  constexpr int STAGE = SparseCfg<D>::kStage;
+  constexpr int STAGES = SparseCfg<D, NT>::kStages;
+  constexpr int ROW = SparseCfg<D, NT>::kRow;
+  constexpr int TILE = SparseCfg<D, NT>::kTile;
+  constexpr int STAGE = SparseCfg<D, NT>::kStage;
   constexpr int QROW = 2 * D + 16;
   using Tile = PaddedTile<D>;
 
@@ -71,7 +79,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* stage_area = smem;
-  uint8_t* qs = smem + SparseCfg<D>::kStageBytes;
+  uint8_t* qs = smem + SparseCfg<D, NT>::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(qs + NPAD * QROW);
   uint64_t* recv_bar = bars + W * STAGES;   // completes when every peer's state has landed
   int32_t* rows = reinterpret_cast<int32_t*>(recv_bar + 1);
@@ -90,7 +98,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   // every CTA has arrived).
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   griddep_begin();
-  float* pM = reinterpret_cast<float*>(rows + SparseCfg<D>::kMaxRows);   // [NPAD] CTA partial
+  float* pM = reinterpret_cast<float*>(rows + SparseCfg<D, NT>::kMaxRows);   // [NPAD] CTA partial
   float* pL = pM + NPAD;                                                 // [NPAD]
   float* pO = pL + NPAD;                                                 // [NPAD][D]
   float* rO = pO + NPAD * D;                     // [CL][per] output slices received
@@ -105,7 +113,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   // The selected positions of this CTA's range are requested together with
   // k_b and the tail (entries past k_b are replaced below), so the index and
   // length loads take one round trip.
-  constexpr int kPer = SparseCfg<D>::kMaxRows / NTH;
+  constexpr int kPer = SparseCfg<D, NT>::kMaxRows / NTH;
   const int rbeg = rank * p.rows_per_split;
   int pos[kPer];
 #pragma unroll
@@ -247,7 +255,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   }
   reduce_row_sums<D, NT>(st);
   __syncthreads();
-  cta_merge_to_smem<D, NT, W>(st, stage_area, SparseCfg<D>::kStageBytes, p.group, pM, pL, pO);
+  cta_merge_to_smem<D, NT, W>(st, stage_area, SparseCfg<D, NT>::kStageBytes, p.group, pM, pL, pO);
 
   // Cluster merge: CTA r owns the output elements [r * per, (r + 1) * per) of
   // the G x D.  Every CTA pushes the slices of its state to their owners'
