@@ -29,16 +29,18 @@ namespace vegas {
 
 template <int D, int NT>
 struct SparseCfg {
-  // 16-row groups in flight per warp: four at head_dim 64 (a group is half
-  // the bytes of a head_dim-128 one), three at head_dim 128 with one column
-  // tile (measured 1-2% faster than two), two with two column tiles (three do
-  // not fit the shared memory there)
-  static constexpr int kStages = D == 64 ? 4 : (NT == 1 ? 3 : 2);
+  // Warps, and 16-row groups in flight per warp: at head_dim 64 (a group is
+  // half the bytes of a head_dim-128 one) sixteen warps with two groups each
+  // (measured 3% faster than eight with four); at head_dim 128 eight warps,
+  // three groups with one column tile (1-2% faster than two), two with two
+  // column tiles (three do not fit the shared memory there)
+  static constexpr int kWarps = D == 64 ? 16 : kAttnWarps;
+  static constexpr int kStages = D == 64 ? 2 : (NT == 1 ? 3 : 2);
   static constexpr int kRow = D * 2 + 16;           // padded row stride
   static constexpr int kTile = 16 * kRow;
   static constexpr int kStage = 2 * kTile;
   static constexpr int kMaxRows = kMaxSparseRowsPerCta;
-  static constexpr size_t kStageBytes = size_t(kAttnWarps) * kStages * kStage;
+  static constexpr size_t kStageBytes = size_t(kWarps) * kStages * kStage;
 };
 
 template <int D, int NT>
@@ -46,7 +48,7 @@ constexpr size_t sparse_smem_layout_bytes() {
   using Cfg = SparseCfg<D, NT>;
   return Cfg::kStageBytes                                          // stages
          + size_t(NT) * 8 * (2 * D + 16)                           // Q tile
-         + (size_t(kAttnWarps) * Cfg::kStages + 1) * 8             // mbarriers (+ receive)
+         + (size_t(Cfg::kWarps) * Cfg::kStages + 1) * 8            // mbarriers (+ receive)
          + size_t(Cfg::kMaxRows) * 4                               // row table
          + size_t(NT) * 8 * (D + 2) * 4                            // CTA partial
          + (size_t(NT) * 8 * D + kMaxSparseCluster) * 4            // received output slices
@@ -60,8 +62,9 @@ static_assert(sparse_smem_layout_bytes<128, 1>() <= 227 * 1024 &&
               "shared memory of a draft CTA");
 
 template <int D, int NT>
-__global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const SparseParams p) {
-  constexpr int W = kAttnWarps;
+__global__ void __launch_bounds__(SparseCfg<D, NT>::kWarps * 32, 1)
+    sparse_decode_kernel(const SparseParams p) {
+  constexpr int W = SparseCfg<D, NT>::kWarps;
   constexpr int NTH = W * 32;
   constexpr int NPAD = NT * 8;
   constexpr int STAGES = SparseCfg<D, NT>::kStages;
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) sparse_decode_kernel(const
   // The selected positions of this CTA's range are requested together with
   // k_b and the tail (entries past k_b are replaced below), so the index and
   // length loads take one round trip.
-  constexpr int kPer = SparseCfg<D, NT>::kMaxRows / NTH;
+  constexpr int kPer = (SparseCfg<D, NT>::kMaxRows + NTH - 1) / NTH;   // entries a thread
   const int rbeg = rank * p.rows_per_split;
   int pos[kPer];
 #pragma unroll
@@ -337,7 +340,7 @@ static cudaError_t launch_sparse_one(const SparseParams& p, int batch, cudaStrea
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits, p.hkv, batch);
-  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+  cfg.blockDim = dim3(SparseCfg<D, NT>::kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
