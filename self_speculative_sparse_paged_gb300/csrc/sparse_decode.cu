@@ -29,13 +29,14 @@ namespace vegas {
 
 template <int D, int NT>
 struct SparseCfg {
-  // Warps, and 16-row groups in flight per warp: at head_dim 64 (a group is
-  // half the bytes of a head_dim-128 one) sixteen warps with two groups each
-  // (measured 3% faster than eight with four); at head_dim 128 eight warps,
-  // three groups with one column tile (1-2% faster than two), two with two
-  // column tiles (three do not fit the shared memory there)
-  static constexpr int kWarps = D == 64 ? 16 : kAttnWarps;
-  static constexpr int kStages = D == 64 ? 2 : (NT == 1 ? 3 : 2);
+  // Warps, each with two 16-row groups in flight: sixteen at head_dim 64 (a
+  // group is half the bytes of a head_dim-128 one; 3% faster than eight warps
+  // with four groups), twelve at head_dim 128 with one column tile (3% faster
+  // than eight with three), eight with two column tiles (the shared memory
+  // holds no more there).  More warps keep the same bytes in flight with more
+  // groups computed at once.
+  static constexpr int kWarps = D == 64 ? 16 : (NT == 1 ? 12 : kAttnWarps);
+  static constexpr int kStages = 2;
   static constexpr int kRow = D * 2 + 16;           // padded row stride
   static constexpr int kTile = 16 * kRow;
   static constexpr int kStage = 2 * kTile;
