@@ -20,6 +20,7 @@ CASES = {
     "qwen_b2": C2.with_(batch=2, ctx_lo=2999, ctx_hi=4100),
     "gptoss_b2": C4.with_(batch=2, ctx_lo=3000, ctx_hi=3000),
     "group16": T.with_(hq=32, hkv=2, ctx_lo=1200, ctx_hi=1200),
+    "group16_d128": C2.with_(hq=32, hkv=2, ctx_lo=2000, ctx_hi=2000),   # two column tiles at d 128
     "k_equals_L": T.with_(ctx_lo=700, ctx_hi=700, k_abs=700),
     "big_k": C2.with_(hkv=2, hq=8, ctx_lo=30000, ctx_hi=30000, k_pct=10),
 }
