@@ -616,8 +616,8 @@ def measure_workload(w, dev, stream, peak, peak_kind, iters=8, repeats=5):
         "roofline_draft": {
             "kernel": "sparse_decode_kernel", "bytes_per_launch": draft_bytes,
             "frac_back_to_back": round(draft_bytes / (d_b2b * 1e-6) / 1e9 / peak, 4),
-            "frac_stage_events": round(nb["draft"][-1] / (st["draft_us_per_step"] * 1e-6) / 1e9
-                                       / peak, 4)},
+            "frac_stage_events": round(statistics.mean(nb["draft"])
+                                       / (st["draft_us_per_step"] * 1e-6) / 1e9 / peak, 4)},
         "l2": (f"iterations rotate over {replicas} copies of the paged cache" if replicas > 1
                else "one copy of the paged cache, several times the 129 MB L2"),
     }
@@ -968,6 +968,22 @@ def roofline_entry(bytes_per_launch, launch_us, peak, peak_kind, stage_us=None,
     return out
 
 
+def draft_roofline_entry(step_bytes, step_us, stage_us, peak):
+    """The draft kernel's roofline object: the mean algorithmic bytes of one
+    draft step (the steps' tails differ by one position each) over the per-step
+    duration of a graph of back-to-back steps, against the HBM peak; the same
+    bytes over the stage-event duration as context."""
+    d_bytes = int(round(statistics.mean(step_bytes)))
+    return {"kernel": "sparse_decode_kernel", "bound": "hbm", "bytes_per_launch": d_bytes,
+            "duration_us": round(step_us, 3),
+            "frac": round(d_bytes / (step_us * 1e-6) / 1e9 / peak, 4),
+            "duration_source": "CUDA events around a graph of back-to-back draft steps "
+                               "(rotating the KV replicas and the step index) on the "
+                               "launching stream, per step",
+            "stage_events": {"duration_us": round(stage_us, 3),
+                             "frac": round(d_bytes / (stage_us * 1e-6) / 1e9 / peak, 4)}}
+
+
 def base_config(w, lens, kps):
     kv = w.hkv * 4 * w.head_dim * int(lens.sum())
     reps = REPLICAS if kv < 4 * 129e6 else 1
@@ -1055,16 +1071,8 @@ def main():
     line["roofline"] = roofline_entry(nbytes["verify"], vb2b, peak, peak_kind, v_us,
                                       kernel=verify_kernel_name(w))
     # the draft kernel, the same way: per launch back to back, stage events as context
-    d_b2b, d_st = variants["draft_step_us"], stages["draft_us_per_step"]
-    d_bytes = int(round(statistics.mean(nbytes["draft"])))   # the steps' mean (their tails differ)
-    line["roofline_draft"] = {
-        "kernel": "sparse_decode_kernel", "bound": "hbm", "bytes_per_launch": d_bytes,
-        "duration_us": round(d_b2b, 3),
-        "frac": round(d_bytes / (d_b2b * 1e-6) / 1e9 / peak, 4),
-        "duration_source": "CUDA events around a graph of back-to-back draft steps (rotating "
-                           "the KV replicas and the step index) on the launching stream, per step",
-        "stage_events": {"duration_us": round(d_st, 3),
-                         "frac": round(d_bytes / (d_st * 1e-6) / 1e9 / peak, 4)}}
+    line["roofline_draft"] = draft_roofline_entry(nbytes["draft"], variants["draft_step_us"],
+                                                  stages["draft_us_per_step"], peak)
     # the "next" rows, measured the same way on the same workload: collect-all
     # capture, one T shared by all heads, the query-agnostic window selector
     line["variants"] = variants

@@ -61,3 +61,10 @@ def test_percentiles_and_stage_free_helpers():
     assert bench.percentile(xs, 50) == 3.0
     assert bench.percentile(xs, 10) == 1.4 and bench.percentile(xs, 90) == 4.6
     assert bench.verify_kernel_name(configs.QWEN3_8B_B1_32K) == "verify_tc_kernel"
+
+
+def test_draft_roofline_entry_takes_the_mean_step_bytes():
+    r = bench.draft_roofline_entry([100_000_000, 100_000_256, 100_000_512], 10.0, 12.5, 6795.5)
+    assert r["bound"] == "hbm" and r["bytes_per_launch"] == 100_000_256
+    assert math.isclose(r["frac"], 100_000_256 / 10e-6 / 1e9 / 6795.5, rel_tol=1e-3)
+    assert math.isclose(r["stage_events"]["frac"], r["frac"] * 10.0 / 12.5, rel_tol=1e-3)
