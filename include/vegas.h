@@ -230,7 +230,9 @@ vegas_status_t vegas_select_window(const int32_t* ctx_lens, int num_sink, int wi
  *   q, out: device bf16 [batch][num_q_heads][head_dim]
  *   max_tail >= max_b tail_len[b]; k_per_seq[b] + tail_len[b] >= 1.
  * Needs no workspace (the split softmax states merge on chip).
- * Supported: head_dim in {64, 128}, G <= 16, k_max + max_tail <= 16384.
+ * Supported: head_dim in {64, 128}, G <= 16, k_max + max_tail <= 32768
+ * (up to 16 CTAs of 2048 entries each per (sequence, KV head)); larger
+ * sets return VEGAS_ERR_UNSUPPORTED before anything is launched.
  * ---------------------------------------------------------------------- */
 vegas_status_t vegas_sparse_decode_attn(
     const vegas_paged_kv_t* kv, const void* q, void* out, const int32_t* idx,

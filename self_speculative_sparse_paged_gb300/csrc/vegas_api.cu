@@ -612,13 +612,13 @@ VEGAS_API vegas_status_t vegas_sparse_decode_attn(
   if (!std::isfinite(softmax_scale)) return fail(VEGAS_ERR_INVALID_ARG, "softmax_scale not finite");
   const int G = kv->num_q_heads / kv->num_kv_heads;
   if (G > 16) return fail(VEGAS_ERR_UNSUPPORTED, "group size %d (at most 16)", G);
+  if ((long long)k_max + max_tail > vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta)
+    return fail(VEGAS_ERR_UNSUPPORTED, "k_max + max_tail = %lld exceeds %d",
+                (long long)k_max + max_tail, vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta);
   if (batch == 0) return VEGAS_OK;
   int* err = nullptr;
   int sms = 0;
   if ((st = device_info(&err, &sms)) != VEGAS_OK) return st;
-  if (k_max + max_tail > vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta)
-    return fail(VEGAS_ERR_UNSUPPORTED, "k_max + max_tail = %d exceeds %d", k_max + max_tail,
-                vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta);
   const SparsePlan pl = plan_sparse(kv, batch, k_max, max_tail, sms);
   vegas::SparseParams p{};
   p.q = q;
@@ -730,9 +730,9 @@ VEGAS_API vegas_status_t vegas_decode_iteration(
     return fail(VEGAS_ERR_UNSUPPORTED, "(gamma+1)*G = %d query rows exceeds this head_dim's limit",
                 (gamma + 1) * G);
   if (G > 16) return fail(VEGAS_ERR_UNSUPPORTED, "group size %d (at most 16)", G);
-  if (k_max + max_tail > vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta)
-    return fail(VEGAS_ERR_UNSUPPORTED, "k_max + max_tail = %d exceeds %d", k_max + max_tail,
-                vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta);
+  if ((long long)k_max + max_tail > vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta)
+    return fail(VEGAS_ERR_UNSUPPORTED, "k_max + max_tail = %lld exceeds %d",
+                (long long)k_max + max_tail, vegas::kMaxSparseCluster * vegas::kMaxSparseRowsPerCta);
   if ((long long)score_stride > 8ll * vegas::select_max_chunk())
     return fail(VEGAS_ERR_UNSUPPORTED, "score_stride %d exceeds %d", score_stride,
                 8 * vegas::select_max_chunk());

@@ -80,6 +80,10 @@ def test_host_validation_rejects_before_launch(vg):
     with pytest.raises(vg.VegasError) as ei:
         vg.vegas_sparse_decode_attn(kv, 16, 16, 16, 4, 16, 16, 16, 1, 1, 0.1, stream=0)
     assert ei.value.status == 2
+    kv = vg.PagedKV(16, 16, 16, 1, 16, 8, 2, 128, 1)    # 32769 draft entries
+    with pytest.raises(vg.VegasError) as ei:
+        vg.vegas_sparse_decode_attn(kv, 16, 16, 16, 32760, 16, 16, 16, 9, 1, 0.1, stream=0)
+    assert ei.value.status == 2
     kv = vg.PagedKV(16, 16, 16, 1, 16, 64, 2, 128, 1)   # (gamma+1)*G = 5*32 rows
     with pytest.raises(vg.VegasError) as ei:
         vg.vegas_verify_attn_capture(kv, 16, 16, None, 0, 16, 1, 4, 0, 4, 0.125, None, 0,

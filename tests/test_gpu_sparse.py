@@ -9,7 +9,7 @@ if not torch.cuda.is_available():
 import oracle  # noqa: E402
 import self_speculative_sparse_paged_gb300 as vg  # noqa: E402
 from vegas_case import Case, assert_attention_close, bf16_to_f64, to_dev  # noqa: E402
-from workload import configs  # noqa: E402
+from workload import configs, gen  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +43,25 @@ def test_sparse_matches_oracle(name):
         ref = oracle.sparse_decode(c.qd_f64()[j], kf, vf, c.pm.block_table, idx, c.kps, c.lens,
                                    np.full(c.w.batch, tl), c.scale)
         assert_attention_close(bf16_to_f64(out), ref, f"draft step {j}")
+
+
+@pytest.mark.parametrize("rows", [16384, 32768])
+def test_sparse_at_the_largest_attention_sets(rows):
+    """k_per_seq + tail up to the call's limit (32768 entries: sixteen CTAs with
+    full row tables at the limit, 1024 entries each at half of it), on random
+    distinct positions of a 33K prefix."""
+    w = C2.with_(batch=1, hq=4, hkv=1, ctx_lo=33000, ctx_hi=33000)
+    c = Case(w)
+    tl = gen.tail_len(w, 0)
+    k = rows - tl
+    rng = np.random.default_rng(rows)
+    idx = np.sort(rng.choice(int(c.lens[0]), size=k, replace=False)).astype(np.int32)
+    idx = idx.reshape(1, 1, k)
+    out = c.sparse(0, to_dev(idx), k_per_seq=[k])
+    kf, vf = c.caches_f64()
+    ref = oracle.sparse_decode(c.qd_f64()[0], kf, vf, c.pm.block_table, idx, np.array([k]),
+                               c.lens, np.array([tl]), c.scale)
+    assert_attention_close(bf16_to_f64(out), ref, f"{rows} entries")
 
 
 def test_sparse_full_prefix_reduces_to_verify_rows():
