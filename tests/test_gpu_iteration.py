@@ -31,7 +31,8 @@ def _gpu_iteration(c: Case):
     configs.TINY,
     configs.QWEN3_8B_B8_48K_64K.with_(batch=2, ctx_lo=3000, ctx_hi=5000),
     configs.GPTOSS_20B_B4_128K.with_(batch=2, ctx_lo=6000, ctx_hi=6000),
-], ids=["tiny", "qwen_b2", "gptoss_b2"])
+    configs.QWEN3_8B_B1_32K.with_(hq=16, hkv=8, gamma=15, ctx_lo=2000, ctx_hi=2000),
+], ids=["tiny", "qwen_b2", "gptoss_b2", "qwen_gamma15_g2"])
 def test_small_iteration_matches_oracle(w):
     c = Case(w)
     out_v, scores, idx, drafts = _gpu_iteration(c)

@@ -35,6 +35,10 @@ SMALL = {
     "tc_ticket_b13": C3.with_(batch=13, ctx_lo=600, ctx_hi=900),           # 104 units: workspace merge
     "gptoss_b5_ragged": C4.with_(batch=5, ctx_lo=3000, ctx_hi=9000),      # 40 units, 3-CTA clusters
     "gptoss_b3_short": C4.with_(batch=3, ctx_lo=1, ctx_hi=700),           # a few tiles a unit
+    "gamma15_g2": C2.with_(hq=16, hkv=8, gamma=15, ctx_lo=1000, ctx_hi=1000),   # largest gamma
+    "gptoss_gamma15_g3": C4.with_(batch=1, hq=24, hkv=8, gamma=15, ctx_lo=900, ctx_hi=900),
+    "g16_gamma1": C2.with_(hq=32, hkv=2, gamma=1, ctx_lo=1500, ctx_hi=1500),   # 16 heads a group
+    "gptoss_g16_gamma2": C4.with_(batch=1, hq=32, hkv=2, gamma=2, ctx_lo=1500, ctx_hi=1500),
 }
 
 
