@@ -28,7 +28,8 @@ def _run(scores32: np.ndarray, lens, kps, k_max, stride=None):
 
 @pytest.mark.parametrize("L,k", [(1, 1), (5, 2), (1000, 0), (1000, 1000), (1000, 37),
                                  (4097, 205), (32768, 1639), (65536, 3277), (131072, 3933),
-                                 (262144, 5000)])
+                                 (262144, 5000), (65537, 60000), (131072, 131071),
+                                 (131072, 131072), (262144, 262143)])
 def test_select_random_scores(L, k):
     rng = np.random.default_rng(L + k)
     s = (rng.standard_normal((2, 3, L)) * 3).astype(np.float32)
