@@ -52,7 +52,7 @@ constexpr size_t sparse_smem_layout_bytes() {
          + (size_t(Cfg::kWarps) * Cfg::kStages + 1) * 8            // mbarriers (+ receive)
          + size_t(Cfg::kMaxRows) * 4                               // row table
          + size_t(NT) * 8 * (D + 2) * 4                            // CTA partial
-         + (size_t(NT) * 8 * D + kMaxSparseCluster) * 4            // received output slices
+         + (size_t(NT) * 8 * D + 4 * kMaxSparseCluster) * 4 + 16   // received output slices
          + size_t(kMaxSparseCluster) * NT * 8 * 2 * 4              // received m, l
          + 1024;
 }
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(SparseCfg<D, NT>::kWarps * 32, 1)
   uint64_t* recv_bar = bars + W * STAGES;   // completes when every peer's state has landed
   int32_t* rows = reinterpret_cast<int32_t*>(recv_bar + 1);
   const int nel = p.group * D;              // output elements of the unit (G x D)
-  const int per = (nel + CL - 1) / CL;      // CTA r owns [r * per, (r + 1) * per)
+  const int per = ((nel + CL - 1) / CL + 3) & ~3;   // CTA r owns [r * per, (r + 1) * per); 4 | per
   if (threadIdx.x == 0) {
     // Every CTA sends this one its slice of the partial output and its G row
     // maxima and sums: 4 * CL * (slice + 2G) bytes, counted by st.async.
@@ -105,8 +105,11 @@ __global__ void __launch_bounds__(SparseCfg<D, NT>::kWarps * 32, 1)
   float* pM = reinterpret_cast<float*>(rows + SparseCfg<D, NT>::kMaxRows);   // [NPAD] CTA partial
   float* pL = pM + NPAD;                                                 // [NPAD]
   float* pO = pL + NPAD;                                                 // [NPAD][D]
-  float* rO = pO + NPAD * D;                     // [CL][per] output slices received
-  float* rM = rO + NPAD * D + kMaxSparseCluster; // [CL][NPAD] maxima received
+  // [CL][per] output slices received (16-byte aligned: they arrive in 16-byte stores;
+  // CL * per <= G * D + 4 * CL - 1)
+  float* rO = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(pO + NPAD * D) + 15) &
+                                       ~uintptr_t(15));
+  float* rM = rO + NPAD * D + 4 * kMaxSparseCluster;   // [CL][NPAD] maxima received
   float* rL = rM + kMaxSparseCluster * NPAD;     // [CL][NPAD] row sums received
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -260,31 +263,36 @@ __global__ void __launch_bounds__(SparseCfg<D, NT>::kWarps * 32, 1)
   reduce_row_sums<D, NT>(st);
   __syncthreads();
   cta_merge_to_smem<D, NT, W>(st, stage_area, SparseCfg<D, NT>::kStageBytes, p.group, pM, pL, pO);
+  __syncthreads();   // the pushes below read elements other threads merged
 
   // Cluster merge: CTA r owns the output elements [r * per, (r + 1) * per) of
-  // the G x D.  Every CTA pushes the slices of its state to their owners'
-  // receive areas with asynchronous distributed-shared-memory stores (each
-  // thread the elements it merged above, threads n < G the row maxima and
-  // sums), each counted against the owner's receive barrier; an owner merges
-  // as soon as its barrier has counted every byte it expects:
+  // the G x D (per a multiple of four).  Every CTA pushes the slices of its
+  // state to their owners' receive areas with asynchronous distributed-
+  // shared-memory stores, 16 bytes each (four elements of one owner), and its
+  // G row maxima and sums to every CTA, one (CTA, row) pair a thread; each
+  // store counts against the owner's receive barrier, and an owner merges as
+  // soon as that barrier has counted every byte it expects:
   // M = max_r m_r, O = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r.
-  // The receive areas are used by nothing else, so only the barrier phase
-  // begun at entry (every CTA has started, its receive barrier is ready)
-  // precedes the stores, and no cluster barrier follows them.
+  // Spreading the pushes over the threads (rather than one thread a row
+  // looping over the CTAs, four bytes a store) took the batch-1 step from
+  // 5.75 to 5.3 us.  The receive areas are used by nothing else, so only the
+  // barrier phase begun at entry (every CTA has started, its receive barrier
+  // is ready) precedes the stores, and no cluster barrier follows them.
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   {
     const uint32_t rO_s = smem_u32(rO), rM_s = smem_u32(rM), rL_s = smem_u32(rL);
     const uint32_t rb = smem_u32(recv_bar);
-    for (int e = tid; e < nel; e += NTH) {
-      const int owner = e / per;
-      st_async_f32(cluster_map(rO_s + 4 * (rank * per + e - owner * per), owner), pO[e],
-                   cluster_map(rb, owner));
+    for (int e = 4 * tid; e < nel; e += 4 * NTH) {   // 4 | nel (D is 64 or 128)
+      const int owner = e / per;                      // e .. e + 3 share it
+      st_async_f32x4(cluster_map(rO_s + 4 * (rank * per + e - owner * per), owner), pO[e],
+                     pO[e + 1], pO[e + 2], pO[e + 3], cluster_map(rb, owner));
     }
-    if (tid < p.group) {
-      for (int r = 0; r < CL; ++r) {
-        st_async_f32(cluster_map(rM_s + 4 * (rank * NPAD + tid), r), pM[tid], cluster_map(rb, r));
-        st_async_f32(cluster_map(rL_s + 4 * (rank * NPAD + tid), r), pL[tid], cluster_map(rb, r));
-      }
+    static_assert(kMaxSparseCluster * 16 <= NTH, "one (CTA, row) pair a thread");
+    const int t = NTH - 1 - tid;   // the last threads, which carry fewer elements
+    if (t < CL * p.group) {        // CL * G <= 256 <= NTH
+      const int r = t / p.group, n = t - r * p.group;
+      st_async_f32(cluster_map(rM_s + 4 * (rank * NPAD + n), r), pM[n], cluster_map(rb, r));
+      st_async_f32(cluster_map(rL_s + 4 * (rank * NPAD + n), r), pL[n], cluster_map(rb, r));
     }
   }
   if (!mbar_wait_cluster_bounded(smem_u32(recv_bar), 0)) {

@@ -310,6 +310,14 @@ __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t re
                "f"(v), "r"(remote_bar)
                : "memory");
 }
+// The same for four consecutive floats (16 bytes; addr 16-byte aligned).
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float a, float b, float c, float d,
+                                               uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+      : "memory");
+}
 // mbar_wait_for at cluster scope: the phase's completion was caused by other
 // CTAs of the cluster (remote transaction counts), whose writes it makes visible.
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity) {
