@@ -56,15 +56,15 @@ def read_peaks():
 
 # DRAM traffic of one verify launch (dram__bytes_read.sum + dram__bytes_write.sum)
 # on this workload, from a one-pass ncu capture of five consecutive verify
-# launches of `python bench.py --profile --steps 8 --warmup 3` (134.42 MB read,
-# 0.47-0.86 MB written per launch); reported only while
+# launches of `python bench.py --profile --steps 8 --warmup 3` (134.41 MB read,
+# 0.45-0.59 MB written per launch after the first); reported only while
 # the kernel sources still hash to the digest they had when the counters were
 # taken.
 VERIFY_TRAFFIC = {
-    "bytes": 135_100_000,
+    "bytes": 134_900_000,
     "sources": ["verify_tc.cu", "split_merge.cuh", "attn_core.cuh", "vegas_common.cuh",
                 "kernels.h"],
-    "sha256": "a3f69b7ee626b449718abd19bdce9a340773a941953e9fc0c4cc69de9cd85269",
+    "sha256": "524ac9623fb81b6890c125b27ae58a67d58ddc1b80bbd7dd890f37d338483a8c",
 }
 
 
