@@ -430,17 +430,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const Selec
     }
     __syncthreads();
     // super-bin sums: thread t adds bins 4t .. 4t + 3, the eight threads of a
-    // super-bin reduce with shuffles, and the first pushes the sum into every
-    // CTA's su[rank][.]
+    // super-bin reduce with shuffles (each ends with the sum), and thread q of
+    // the eight pushes it into CTA q's su[rank][.]: one remote store a thread
+    // rather than one thread looping over the CTAs
     static_assert(4 * kSelThreads == kBins && kFine == 32, "four bins a thread");
+    static_assert(kMaxSelCluster <= 8, "one CTA per thread of a super-bin");
     {
       const uint4 c4 = *reinterpret_cast<const uint4*>(c + 4 * tid);
       uint32_t x = c4.x + c4.y + c4.z + c4.w;
       x += __shfl_xor_sync(0xffffffffu, x, 1);
       x += __shfl_xor_sync(0xffffffffu, x, 2);
       x += __shfl_xor_sync(0xffffffffu, x, 4);
-      if ((tid & 7) == 0)
-        for (int q = 0; q < CL; ++q) cluster.map_shared_rank(su, q)[rank * kSuper + (tid >> 3)] = x;
+      if ((tid & 7) < CL) cluster.map_shared_rank(su, tid & 7)[rank * kSuper + (tid >> 3)] = x;
     }
     cluster.sync();
     // The other set's last readers (the previous level's search) are past
