@@ -690,6 +690,27 @@ def measure_stack(w, dev, stream, peak, peak_kind, repeats=3):
     return out
 
 
+# The metric's range at full depth: (gamma, k%) from the lightest to the
+# heaviest draft phase, and the point the bench line reports.
+STACK_SWEEP = ((2, 3), (2, 10), (4, 5), (8, 3), (8, 10))
+
+
+def stack_sweep(peak, peak_kind):
+    """The 36-layer Qwen3-8B stack (batch 4, 96K-120K) at each STACK_SWEEP point:
+    one measure_stack result a point, with the clocks sampled while it ran."""
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    for gamma, k_pct in STACK_SWEEP:
+        w = configs.QWEN3_8B_36L_B4_96K_120K.with_(gamma=gamma, k_pct=k_pct)
+        sampler = ClockSampler(dev.index)
+        sampler.start()
+        out = measure_stack(w, dev, stream, peak, peak_kind)
+        out["clocks"] = sampler.stop()
+        yield out
+
+
 def run_gpu(args, rank, world, dist, peak, peak_kind):
     import torch
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
@@ -1006,6 +1027,9 @@ def main():
                     help="only the headline workload (no extra workloads)")
     ap.add_argument("--profile", action="store_true",
                     help="timed region, stages and back-to-back verify/select only (profiler runs)")
+    ap.add_argument("--stack-sweep", action="store_true",
+                    help="only the 36-layer stack at the corners of the (gamma, k) range, "
+                         "one JSON line per point")
     ap.add_argument("--workload", default=WORKLOAD.name, choices=sorted(configs.BY_NAME),
                     help="the headline workload (default: the Qwen3-8B layer, batch 1, 32K)")
     args = ap.parse_args()
@@ -1038,6 +1062,11 @@ def main():
         print(json.dumps(line))
         return
 
+    if args.stack_sweep:
+        if rank == 0:
+            for line in stack_sweep(peak, peak_kind):
+                print(json.dumps(line), flush=True)
+        return
     dist = None
     if world > 1:
         import torch.distributed as tdist
