@@ -23,6 +23,9 @@ CASES = {
     "group16_d128": C2.with_(hq=32, hkv=2, ctx_lo=2000, ctx_hi=2000),   # two column tiles at d 128
     "k_equals_L": T.with_(ctx_lo=700, ctx_hi=700, k_abs=700),
     "big_k": C2.with_(hkv=2, hq=8, ctx_lo=30000, ctx_hi=30000, k_pct=10),
+    # one query head a KV head at head_dim 64: 64 output elements over a large cluster,
+    # so some CTAs own none of them and receive only the row maxima and sums
+    "mha_g1_wide_cluster": T.with_(hq=4, hkv=4, ctx_lo=10000, ctx_hi=10000, k_abs=760),
 }
 
 
