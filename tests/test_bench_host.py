@@ -68,3 +68,19 @@ def test_draft_roofline_entry_takes_the_mean_step_bytes():
     assert r["bound"] == "hbm" and r["bytes_per_launch"] == 100_000_256
     assert math.isclose(r["frac"], 100_000_256 / 10e-6 / 1e9 / 6795.5, rel_tol=1e-3)
     assert math.isclose(r["stage_events"]["frac"], r["frac"] * 10.0 / 12.5, rel_tol=1e-3)
+
+
+def test_stack_sweep_bytes_follow_the_closed_form():
+    """Per iteration of the 36-layer stack the path reads every prefix K/V row once
+    for verify and a fraction gamma * r of them again over the draft steps, and
+    writes then reads one fp32 score per (position, KV head):
+    layers * (Hkv * 4d * sum L_b * (1 + gamma * r) + 8 * Hkv * sum L_b).  The
+    accounting adds only queries, outputs, indices and the dense tails (< 1%)."""
+    for gamma, k_pct in bench.STACK_SWEEP:
+        w = configs.QWEN3_8B_36L_B4_96K_120K.with_(gamma=gamma, k_pct=k_pct)
+        lens = gen.ctx_lens(w)
+        nb = bench.algorithmic_bytes(w, lens, gen.k_per_seq(w, lens))
+        s = int(lens.sum())
+        closed = w.layers * (w.hkv * 4 * w.head_dim * s * (1 + gamma * k_pct / 100)
+                             + 8 * w.hkv * s)
+        assert 1.0 <= nb["total"] * w.layers / closed < 1.01, (gamma, k_pct)
