@@ -343,6 +343,45 @@ def test_sparse_closed_forms():
         np.testing.assert_allclose(o0[b], V[b, np.arange(4) // 2, int(lens[b])], atol=1e-14)
 
 
+def test_sparse_does_not_depend_on_the_order_of_the_selected_positions():
+    """T is a set (the §2.A argmax is over subsets): any order of its indices
+    gives the same draft output."""
+    rng = np.random.default_rng(12)
+    q, K, V, kc, vc, bt, lens = _rand_case(rng)
+    B = q.shape[0]
+    k = 9
+    idx = np.zeros((B, 2, k + 2), dtype=np.int32)
+    for b in range(B):
+        for g in range(2):
+            idx[b, g, :k] = np.sort(rng.choice(int(lens[b]), size=k, replace=False))
+    o = oracle.sparse_decode(q[:, 1], kc, vc, bt, idx, np.full(B, k), lens, np.full(B, 4), 0.4)
+    perm = idx.copy()
+    for b in range(B):
+        for g in range(2):
+            perm[b, g, :k] = rng.permutation(perm[b, g, :k])
+    assert not np.array_equal(perm, idx)
+    o2 = oracle.sparse_decode(q[:, 1], kc, vc, bt, perm, np.full(B, k), lens, np.full(B, 4), 0.4)
+    np.testing.assert_allclose(o2, o, atol=1e-13)
+
+
+def test_attention_is_affine_in_v():
+    """Softmax weights are non-negative and sum to one, so replacing V by
+    a * V + c maps every output o to a * o + c (verify rows and draft rows)."""
+    rng = np.random.default_rng(13)
+    q, K, V, kc, vc, bt, lens = _rand_case(rng)
+    sc = 1 / math.sqrt(8)
+    a, c = -1.75, 0.625
+    o = oracle.verify_attention(q, kc, vc, bt, lens, sc)
+    o2 = oracle.verify_attention(q, kc, a * vc + c, bt, lens, sc)
+    np.testing.assert_allclose(o2, a * o + c, atol=1e-12)
+    B = q.shape[0]
+    idx = np.tile(np.arange(6, dtype=np.int32) * 3, (B, 2, 1))
+    d1 = oracle.sparse_decode(q[:, 0], kc, vc, bt, idx, np.full(B, 6), lens, np.full(B, 2), sc)
+    d2 = oracle.sparse_decode(q[:, 0], kc, a * vc + c, bt, idx, np.full(B, 6), lens,
+                              np.full(B, 2), sc)
+    np.testing.assert_allclose(d2, a * d1 + c, atol=1e-12)
+
+
 def test_iteration_dense_selection_reduces_to_dense_draft():
     """r = 100%: every draft step equals dense attention over [0, L_b + gamma + 2 + j)."""
     rng = np.random.default_rng(12)
